@@ -1,0 +1,123 @@
+"""FP64 CPU oracle for ``C = act(A @ B + bias)`` (FP16 in, FP16 out).
+
+TEST INFRASTRUCTURE ONLY: the plain, slow, obviously correct definition that the CUDA
+kernels are checked against. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline legs of ``bench.py`` may import it; the library's product path never does. It
+shares no code with the CUDA path (its arithmetic lives in ``oracle.c``, compiled with the
+host C compiler; this module only builds it and marshals arguments).
+
+Every function is pinned by ``tests/test_oracle.py``; see the header of ``oracle.c`` for
+what is computed and which passage of the tutorial pages each part follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ACT_NONE, ACT_GELU, ACT_RELU = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` beside it (host C compiler only)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O3", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC,
+               "-lm", "-lpthread"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_half_to_double.restype = ctypes.c_double
+            lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_double_to_half.restype = ctypes.c_uint16
+            lib.oracle_double_to_half.argtypes = [ctypes.c_double]
+            lib.oracle_act.restype = ctypes.c_double
+            lib.oracle_act.argtypes = [ctypes.c_double, ctypes.c_int]
+            lib.oracle_default_threads.restype = ctypes.c_int
+            lib.oracle_gemm_rows.restype = ctypes.c_int
+            lib.oracle_gemm_rows.argtypes = [
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+            _lib = lib
+    return _lib
+
+
+def half_to_double(bits: int) -> float:
+    return _load().oracle_half_to_double(int(bits))
+
+
+def double_to_half(x: float) -> int:
+    return int(_load().oracle_double_to_half(float(x)))
+
+
+def act(x: float, code: int) -> float:
+    return _load().oracle_act(float(x), int(code))
+
+
+def default_threads() -> int:
+    return int(_load().oracle_default_threads())
+
+
+def _u16(t) -> np.ndarray:
+    """FP16 data (numpy float16/uint16 array or CPU torch.float16 tensor) as uint16 bits."""
+    if t is None:
+        return None
+    if hasattr(t, "detach"):  # torch tensor
+        t = t.detach().cpu().contiguous().view(dtype=__import__("torch").int16).numpy()
+    a = np.ascontiguousarray(t)
+    if a.dtype == np.float16 or a.dtype == np.int16:
+        a = a.view(np.uint16)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected FP16 bits, got {a.dtype}")
+    return a
+
+
+def gemm(A, B, bias=None, act_code: int = ACT_NONE, rows=None, threads: int = 0,
+         want_f64: bool = False):
+    """Oracle ``act(A @ B + bias)`` for the given output rows (all rows when ``rows`` is None).
+
+    ``A`` is M x K and ``B`` K x N FP16 (numpy float16/uint16 or CPU torch.float16);
+    ``bias`` has N entries or is None. Returns ``(out_fp16 [nrows, N] as numpy float16,
+    out_f64 [nrows, N] or None, threads_used)``.
+    """
+    a, b, bi = _u16(A), _u16(B), _u16(bias)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError(f"shape mismatch {a.shape} @ {b.shape}")
+    M, K = a.shape
+    N = b.shape[1]
+    if bi is not None and bi.shape != (N,):
+        raise ValueError(f"bias must have {N} entries")
+    if rows is None:
+        r = None
+        nrows = M
+    else:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = r.shape[0]
+    out_h = np.empty((nrows, N), dtype=np.uint16)
+    out_d = np.empty((nrows, N), dtype=np.float64) if want_f64 else None
+    used = ctypes.c_int(0)
+    rc = _load().oracle_gemm_rows(
+        M, N, K, a.ctypes.data, b.ctypes.data, None if bi is None else bi.ctypes.data,
+        int(act_code), None if r is None else r.ctypes.data, nrows, out_h.ctypes.data,
+        None if out_d is None else out_d.ctypes.data, int(threads), ctypes.byref(used))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_rows failed with code {rc}")
+    return out_h.view(np.float16), out_d, used.value
