@@ -1,0 +1,133 @@
+/*
+ * gemm.h - C ABI of the GB300 (sm_103a) FP16 tensor-core GEMM with a fused epilogue.
+ *
+ *     C = act(A * B + bias)        A: M x K, B: K x N, C: M x N, all FP16, row-major
+ *
+ * The operation is the tensor-core GEMM of the TileLang tutorial pages:
+ *  - "TileLang: Criando Kernels de GPU de Alto Desempenho ..." (noticiai.com.br), section
+ *    "GEMM com Tensor Cores: onde a magica acontece": a tiled matrix multiply whose caller
+ *    passes A, B, C and M, N, K (tiled_gemm(A, B, C, M, N, K)); tiles A[i:i+128, k:k+32]
+ *    and B[k:k+32, j:j+128], i.e. A is M x K and B is K x N, both row-major.
+ *  - same page, section "GEMM com epilogo fundido: ReLU e bias 'de graca'": ReLU (and, by
+ *    the same pattern, bias and GELU) applied to the accumulator inside the one kernel,
+ *    with no extra pass over C in DRAM.
+ *  - "TileLang ..." (pro.edgex.exchange), fused-epilogue paragraph: bias addition, then
+ *    GELU, on the register-resident accumulator before the output store.
+ *  - "Designing High-Performance GPU Kernels with TileLang" (spaxe.top), GEMM paragraph:
+ *    FP16 matrix multiplication on tensor cores.
+ * Arithmetic: FP16 inputs, FP32 accumulation in Tensor Memory, epilogue in FP32 (bias is
+ * added first, then the activation; GELU is the exact-erf form 0.5*x*(1+erf(x/sqrt(2)))),
+ * one round-to-nearest-even conversion to FP16, one store.
+ *
+ * Threading: a context may be used by one host thread at a time (or with external
+ * serialisation). Calls on different contexts are independent.
+ */
+#ifndef GB300_GEMM_H
+#define GB300_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque context: cached device properties, the tensor-map encoder, a 4-byte device
+ * error word and (only once gemm_run_host has been called) host-path staging buffers. */
+typedef struct gemm_ctx gemm_ctx;
+
+/* Epilogue selector. The bias is applied whenever `bias` is non-NULL, for every value. */
+enum gemm_epilogue {
+    GEMM_EPI_NONE = 0, /* C = A*B (+ bias)                                           */
+    GEMM_EPI_GELU = 1, /* C = GELU_erf(A*B (+ bias))                                 */
+    GEMM_EPI_RELU = 2  /* C = max(A*B (+ bias), 0)                                   */
+};
+
+/* Status codes. Every error is detected before anything is enqueued: on error nothing
+ * has been launched or copied, except for GEMM_ERR_LAUNCH, which wraps a CUDA error
+ * reported by the launch itself. */
+enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_ARG = -1,     /* NULL context or buffer, negative or too large size,
+                              epilogue out of range                                   */
+    GEMM_ERR_ALIGN = -2,   /* a pointer not 16-byte aligned, or N or K not a multiple of
+                              8 (row strides must be multiples of 16 bytes)           */
+    GEMM_ERR_DEVICE = -3,  /* no such device, not compute capability 10.3, or a buffer
+                              that is not device memory of the context's device       */
+    GEMM_ERR_LAUNCH = -4,  /* a CUDA runtime call failed (see gemm_last_cuda_error)   */
+    GEMM_ERR_TIMEOUT = -5, /* a bounded in-kernel wait ran out; the kernel returned
+                              early and C is incomplete (see gemm_last_device_error) */
+    GEMM_ERR_NOMEM = -6    /* host or device allocation failed (create, run_host)     */
+};
+
+/* Create a context for CUDA device `device` (0-based). Checks that the device has compute
+ * capability 10.3 (GB300, sm_103a), reads its SM count, sets the kernel's shared-memory
+ * attribute, resolves cuTensorMapEncodeTiled and allocates the 4-byte device error word.
+ * On success *out receives the context (caller frees it with gemm_destroy) and GEMM_OK is
+ * returned; on failure *out is set to NULL. The caller's current device is left as it was. */
+int gemm_create(gemm_ctx **out, int device);
+
+/* Enqueue C = act(A*B + bias) on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream) and return without waiting.
+ *   M, N, K : sizes, 0 <= M, N, K <= 2^31 - 1. M = 0 or N = 0 is a no-op (GEMM_OK, nothing
+ *             enqueued). K = 0 gives C = act(bias) (act(0) without a bias). M is
+ *             arbitrary (rows past a tile multiple are masked); N and K must be multiples
+ *             of 8.
+ *   A       : device pointer, M x K FP16 row-major (K contiguous), 16-byte aligned.
+ *   B       : device pointer, K x N FP16 row-major (N contiguous), 16-byte aligned.
+ *             (A and B may be NULL only when K = 0.)
+ *   bias    : device pointer to N FP16 values (16-byte aligned), or NULL for no bias.
+ *   C       : device pointer, M x N FP16 row-major, 16-byte aligned; written, never read.
+ *             C must not overlap A, B or bias.
+ *   epilogue: a gemm_epilogue value.
+ * Ownership: the caller owns every buffer and must keep them alive until the stream has
+ * passed this call. gemm_run allocates nothing and launches exactly one kernel.
+ * Errors: see gemm_status. A wait that runs out inside the kernel is reported later by
+ * gemm_last_device_error, not by this call. */
+int gemm_run(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+             const void *bias, void *C, int epilogue, void *stream);
+
+/* The same operation on HOST buffers (pinned memory gives asynchronous copies; pageable
+ * memory works but is copied synchronously): copies A, B and bias to device staging
+ * buffers owned by the context (allocated or grown on first use, freed by gemm_destroy),
+ * runs gemm_run on `stream`, copies C back to the host buffer and waits for the stream.
+ * Same argument rules as gemm_run, except that the pointers are host pointers. Also
+ * reports a device-side timeout (GEMM_ERR_TIMEOUT) since it synchronises. */
+int gemm_run_host(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A,
+                  const void *B, const void *bias, void *C, int epilogue, void *stream);
+
+/* After the caller has synchronised the stream(s) that ran this context's GEMMs: return
+ * GEMM_OK, or GEMM_ERR_TIMEOUT if a bounded in-kernel wait ran out since the last call.
+ * `detail` (may be NULL) receives the raw error word (which wait ran out: 1 producer
+ * slot, 2 MMA operands, 3 MMA accumulator, 4 epilogue accumulator, 5 teardown drain).
+ * Clears the word. Synchronous (a 4-byte device-to-host copy). */
+int gemm_last_device_error(gemm_ctx *ctx, uint32_t *detail);
+
+/* The last CUDA runtime error code seen by this context (0 if none), for diagnosis of
+ * GEMM_ERR_LAUNCH / GEMM_ERR_NOMEM. */
+int gemm_last_cuda_error(gemm_ctx *ctx);
+
+/* Destroy a context (NULL is accepted). Frees the error word and any staging buffers; the
+ * caller must have synchronised every stream that still runs work of this context. */
+int gemm_destroy(gemm_ctx *ctx);
+
+/* A static, human-readable name for a status code. */
+const char *gemm_status_string(int status);
+
+/* Number of streaming multiprocessors the persistent kernel sizes its grid to. */
+int gemm_num_sms(gemm_ctx *ctx);
+
+/* Test hooks for the failure path (no effect on results when left at their defaults).
+ *   gemm_set_timeout_ns: the limit of every in-kernel wait (default 2e9 ns; values below
+ *     1e6 are raised to 1e6).
+ *   gemm_set_debug: GEMM_DEBUG_WITHHOLD_FIRST_LOAD makes the producer of every CTA hold
+ *     back its first operand load, so that the MMA's wait on it runs out and the kernel
+ *     must take its timeout path (a flag that nothing sets; no fault, no hang). */
+enum { GEMM_DEBUG_NONE = 0, GEMM_DEBUG_WITHHOLD_FIRST_LOAD = 1 };
+int gemm_set_timeout_ns(gemm_ctx *ctx, uint64_t ns);
+int gemm_set_debug(gemm_ctx *ctx, int flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_GEMM_H */

@@ -1,0 +1,352 @@
+// Host side of the C ABI declared in include/gemm.h: argument checks, tensor-map encoding
+// and the launch of the persistent tcgen05 GEMM kernel (gemm_kernel.cuh).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "gemm.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+using Cfg = gb300::KernelConfig<128, 256, 4>;
+constexpr int kGroupM = 16;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr uint64_t kMinTimeoutNs = 1000000ull;
+
+}  // namespace
+
+struct gemm_ctx {
+    int device = -1;
+    int num_sms = 0;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    uint32_t *d_err = nullptr;
+    uint64_t timeout_ns = kDefaultTimeoutNs;
+    int debug = 0;
+    int last_cuda_error = 0;
+    // staging buffers of gemm_run_host
+    void *stage = nullptr;
+    size_t stage_bytes = 0;
+};
+
+namespace {
+
+// Make `device` current for the lifetime of the guard, then restore the caller's device.
+class DeviceGuard {
+  public:
+    explicit DeviceGuard(int device)
+    {
+        if (cudaGetDevice(&prev_) != cudaSuccess) {
+            cudaGetLastError();
+            prev_ = -1;
+        }
+        if (prev_ != device)
+            cudaSetDevice(device);
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev_ >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev_)
+            cudaSetDevice(prev_);
+    }
+
+  private:
+    int prev_ = -1;
+};
+
+int cuda_fail(gemm_ctx *ctx, cudaError_t e, int code)
+{
+    if (ctx)
+        ctx->last_cuda_error = static_cast<int>(e);
+    cudaGetLastError();   // clear the sticky-free error state
+    return code;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// True when p is device (or managed) memory that `device` can address directly.
+bool on_device(const void *p, int device)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeManaged)
+        return true;
+    return a.type == cudaMemoryTypeDevice && a.device == device;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0)
+        return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// Shape/pointer rules shared by gemm_run and gemm_run_host (everything but memory kind).
+int check_args(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+               const void *bias, void *C, int epilogue)
+{
+    if (!ctx)
+        return GEMM_ERR_ARG;
+    if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return GEMM_ERR_ARG;
+    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_RELU)
+        return GEMM_ERR_ARG;
+    if (M == 0 || N == 0)
+        return GEMM_OK;
+    if (!C || (K > 0 && (!A || !B)))
+        return GEMM_ERR_ARG;
+    if (N % 8 != 0 || K % 8 != 0)
+        return GEMM_ERR_ALIGN;
+    if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B))) || (bias && !aligned16(bias)))
+        return GEMM_ERR_ALIGN;
+    const size_t cb = static_cast<size_t>(M) * N * 2;
+    if (overlaps(C, cb, A, static_cast<size_t>(M) * K * 2) ||
+        overlaps(C, cb, B, static_cast<size_t>(K) * N * 2) || overlaps(C, cb, bias, static_cast<size_t>(N) * 2))
+        return GEMM_ERR_ARG;
+    return GEMM_OK;
+}
+
+// 2-D FP16 tensor map over a row-major [outer x inner] matrix, 128-byte swizzled boxes of
+// box_inner x box_outer elements; out-of-range elements read as zero.
+bool encode_2d(gemm_ctx *ctx, CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
+               uint32_t box_inner, uint32_t box_outer)
+{
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims,
+                                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, const void *bias, void *C,
+           int epilogue, cudaStream_t stream)
+{
+    CUtensorMap ta, tb;
+    std::memset(&ta, 0, sizeof(ta));
+    std::memset(&tb, 0, sizeof(tb));
+    if (K > 0) {
+        if (!encode_2d(ctx, &ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), Cfg::BK, Cfg::BM) ||
+            !encode_2d(ctx, &tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), Cfg::B_BOX_N, Cfg::BK))
+            return GEMM_ERR_LAUNCH;
+    }
+    gb300::GemmParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.m_blocks = (M + Cfg::BM - 1) / Cfg::BM;
+    p.n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
+    p.num_tiles = p.m_blocks * p.n_blocks;
+    p.num_kb = (K + Cfg::BK - 1) / Cfg::BK;
+    p.group_m = kGroupM;
+    p.epilogue = epilogue;
+    p.bias = static_cast<const __half *>(bias);
+    p.C = static_cast<__half *>(C);
+    p.err = ctx->d_err;
+    p.timeout_ns = ctx->timeout_ns;
+    p.debug = ctx->debug;
+    const int grid = std::min(p.num_tiles, ctx->num_sms);
+    gb300::gemm_tcgen05_kernel<Cfg><<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_create(gemm_ctx **out, int device)
+{
+    if (!out)
+        return GEMM_ERR_ARG;
+    *out = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_DEVICE;
+    }
+    if (device < 0 || device >= count)
+        return GEMM_ERR_DEVICE;
+    int major = 0, minor = 0, sms = 0, smem_optin = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    if (major != 10 || minor != 3 || sms <= 0 || smem_optin < Cfg::SMEM_BYTES)
+        return GEMM_ERR_DEVICE;
+
+    gemm_ctx *ctx = new (std::nothrow) gemm_ctx();
+    if (!ctx)
+        return GEMM_ERR_NOMEM;
+    ctx->device = device;
+    ctx->num_sms = sms;
+    DeviceGuard guard(device);
+    cudaError_t e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) {
+        delete ctx;
+        return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);
+    }
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        delete ctx;
+        return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);
+    }
+    ctx->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    e = cudaMalloc(&ctx->d_err, sizeof(uint32_t));
+    if (e == cudaSuccess)
+        e = cudaMemset(ctx->d_err, 0, sizeof(uint32_t));
+    if (e != cudaSuccess) {
+        if (ctx->d_err)
+            cudaFree(ctx->d_err);
+        delete ctx;
+        return cuda_fail(nullptr, e, GEMM_ERR_NOMEM);
+    }
+    *out = ctx;
+    return GEMM_OK;
+}
+
+int gemm_run(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, const void *B, const void *bias,
+             void *C, int epilogue, void *stream)
+{
+    int rc = check_args(ctx, M, N, K, A, B, bias, C, epilogue);
+    if (rc != GEMM_OK || M == 0 || N == 0)
+        return rc;
+    if (!on_device(C, ctx->device) || (K > 0 && (!on_device(A, ctx->device) || !on_device(B, ctx->device))) ||
+        (bias && !on_device(bias, ctx->device)))
+        return GEMM_ERR_DEVICE;
+    DeviceGuard guard(ctx->device);
+    return launch(ctx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), A, B, bias, C, epilogue,
+                  static_cast<cudaStream_t>(stream));
+}
+
+int gemm_run_host(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+                  const void *bias, void *C, int epilogue, void *stream)
+{
+    int rc = check_args(ctx, M, N, K, A, B, bias, C, epilogue);
+    if (rc != GEMM_OK || M == 0 || N == 0)
+        return rc;
+    auto round256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t a_b = static_cast<size_t>(M) * K * 2, b_b = static_cast<size_t>(K) * N * 2;
+    const size_t bias_b = bias ? static_cast<size_t>(N) * 2 : 0, c_b = static_cast<size_t>(M) * N * 2;
+    const size_t need = round256(a_b) + round256(b_b) + round256(bias_b) + round256(c_b);
+    DeviceGuard guard(ctx->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (need > ctx->stage_bytes) {
+        if (ctx->stage) {
+            cudaStreamSynchronize(s);
+            cudaFree(ctx->stage);
+            ctx->stage = nullptr;
+            ctx->stage_bytes = 0;
+        }
+        e = cudaMalloc(&ctx->stage, need);
+        if (e != cudaSuccess) {
+            ctx->stage = nullptr;
+            return cuda_fail(ctx, e, GEMM_ERR_NOMEM);
+        }
+        ctx->stage_bytes = need;
+    }
+    char *base = static_cast<char *>(ctx->stage);
+    void *dA = base, *dB = base + round256(a_b);
+    void *dbias = bias ? base + round256(a_b) + round256(b_b) : nullptr;
+    void *dC = base + round256(a_b) + round256(b_b) + round256(bias_b);
+    if (a_b && (e = cudaMemcpyAsync(dA, A, a_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+    if (b_b && (e = cudaMemcpyAsync(dB, B, b_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+    if (bias_b && (e = cudaMemcpyAsync(dbias, bias, bias_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+    rc = launch(ctx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), K ? dA : nullptr,
+                K ? dB : nullptr, dbias, dC, epilogue, s);
+    if (rc != GEMM_OK)
+        return rc;
+    if ((e = cudaMemcpyAsync(C, dC, c_b, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess)
+        return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+    return gemm_last_device_error(ctx, nullptr);
+}
+
+int gemm_last_device_error(gemm_ctx *ctx, uint32_t *detail)
+{
+    if (!ctx)
+        return GEMM_ERR_ARG;
+    DeviceGuard guard(ctx->device);
+    uint32_t w = 0;
+    cudaError_t e = cudaMemcpy(&w, ctx->d_err, sizeof(w), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && w != 0)
+        e = cudaMemset(ctx->d_err, 0, sizeof(uint32_t));
+    if (e != cudaSuccess)
+        return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+    if (detail)
+        *detail = w;
+    return w ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+int gemm_last_cuda_error(gemm_ctx *ctx) { return ctx ? ctx->last_cuda_error : 0; }
+
+int gemm_destroy(gemm_ctx *ctx)
+{
+    if (!ctx)
+        return GEMM_OK;
+    {
+        DeviceGuard guard(ctx->device);
+        if (ctx->d_err)
+            cudaFree(ctx->d_err);
+        if (ctx->stage)
+            cudaFree(ctx->stage);
+        cudaGetLastError();
+    }
+    delete ctx;
+    return GEMM_OK;
+}
+
+const char *gemm_status_string(int status)
+{
+    switch (status) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_ARG: return "GEMM_ERR_ARG: invalid argument";
+    case GEMM_ERR_ALIGN: return "GEMM_ERR_ALIGN: pointer not 16-byte aligned or N, K not multiples of 8";
+    case GEMM_ERR_DEVICE: return "GEMM_ERR_DEVICE: device missing, not sm_103, or buffer not on the device";
+    case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: a CUDA call failed";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: an in-kernel wait ran out";
+    case GEMM_ERR_NOMEM: return "GEMM_ERR_NOMEM: allocation failed";
+    default: return "unknown gemm status";
+    }
+}
+
+int gemm_num_sms(gemm_ctx *ctx) { return ctx ? ctx->num_sms : 0; }
+
+int gemm_set_timeout_ns(gemm_ctx *ctx, uint64_t ns)
+{
+    if (!ctx)
+        return GEMM_ERR_ARG;
+    ctx->timeout_ns = std::max(ns, kMinTimeoutNs);
+    return GEMM_OK;
+}
+
+int gemm_set_debug(gemm_ctx *ctx, int flags)
+{
+    if (!ctx || (flags & ~GEMM_DEBUG_WITHHOLD_FIRST_LOAD))
+        return GEMM_ERR_ARG;
+    ctx->debug = flags;
+    return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,412 @@
+// Persistent, warp-specialised FP16 GEMM with a fused epilogue for sm_103a (GB300):
+//
+//     C[M x N] = act(A[M x K] * B[K x N] + bias[N])      FP16 in, FP32 accumulate, FP16 out
+//
+// The tutorial's tiled tensor-core GEMM ("TileLang: Criando Kernels de GPU ..." on
+// noticiai.com.br, section "GEMM com Tensor Cores": tiles of A and B staged global ->
+// shared, multiplied on tensor cores, the output tile stored once) and its fused epilogue
+// (same page, section "GEMM com epilogo fundido"; "TileLang ..." on pro.edgex.exchange,
+// fused-epilogue paragraph: bias, then GELU, applied to the accumulator before the store),
+// redesigned for the fifth-generation tensor cores:
+//
+//  * one CTA per SM, looping over output tiles in a grouped (L2-friendly) raster;
+//  * warp 0: TMA producer, fills a STAGES-deep ring of 128-byte-swizzled shared-memory
+//    slots (A: BM x 64 K-major; B: 64 x BN as BN/64 boxes of 64 N-columns, MN-major),
+//    gated by full/empty mbarriers;
+//  * warp 1: allocates Tensor Memory and issues tcgen05.mma (M = BM, N = BN, K = 16) from
+//    one thread into one of two FP32 TMEM accumulators, releasing each slot with
+//    tcgen05.commit;
+//  * warps 2..5: epilogue. Each warp owns one 32-lane quarter of TMEM (= 32 rows of the
+//    tile); it reads its rows with tcgen05.ld, adds the bias, applies the activation in
+//    FP32, rounds to FP16 and writes 16-byte vectors, masking rows >= M and columns >= N.
+//    While it drains accumulator b, the MMA warp already fills accumulator b ^ 1.
+//
+// Every mbarrier wait is bounded in time. When a wait runs out the kernel records which
+// one in a device error word, tells the other roles to stop, waits (bounded) for its own
+// copies and MMAs in flight, frees its Tensor Memory and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace gb300 {
+
+// Which wait ran out (the device error word).
+enum : uint32_t {
+    ERR_PRODUCER_SLOT = 1,
+    ERR_MMA_OPERANDS = 2,
+    ERR_MMA_ACCUMULATOR = 3,
+    ERR_EPILOGUE_ACCUMULATOR = 4,
+    ERR_TEARDOWN_DRAIN = 5,
+};
+
+enum : int { EPI_NONE = 0, EPI_GELU = 1, EPI_RELU = 2 };
+enum : int { DEBUG_WITHHOLD_FIRST_LOAD = 1 };
+
+struct GemmParams {
+    int M, N, K;
+    int m_blocks, n_blocks, num_tiles, num_kb;
+    int group_m;           // m-blocks per raster group
+    int epilogue;          // EPI_*
+    const __half *bias;    // N values or nullptr
+    __half *C;             // M x N row-major
+    uint32_t *err;         // device error word
+    uint64_t timeout_ns;   // limit of every wait
+    int debug;             // DEBUG_* flags
+};
+
+template <int BM_, int BN_, int STAGES_>
+struct KernelConfig {
+    static constexpr int BM = BM_;          // rows of A / C per tile (= UMMA M, = TMEM lanes)
+    static constexpr int BN = BN_;          // columns of B / C per tile (= UMMA N)
+    static constexpr int BK = 64;           // K per stage: 64 FP16 = one 128-byte swizzle row
+    static constexpr int UMMA_K = 16;       // K per tcgen05.mma of kind::f16
+    static constexpr int STAGES = STAGES_;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BOX_N = 64;                 // N per TMA box of B (128 bytes)
+    static constexpr int B_BOXES = BN / B_BOX_N;
+    static constexpr int B_BOX_BYTES = BK * B_BOX_N * 2;
+    static constexpr int B_BYTES = BK * BN * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int ACC_BUFS = 2;
+    static constexpr int TMEM_COLS = ACC_BUFS * BN;    // FP32 accumulators, one column each
+    static constexpr int NUM_EPI_WARPS = 4;
+    static constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES +
+                                      NUM_BARS * 8 + 64;
+
+    static_assert(BM == 128, "one CTA, M = 128: TMEM lane i holds tile row i");
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
+    static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM alloc size");
+    static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+};
+
+// UMMA shared-memory descriptor for a 128-byte-swizzled operand tile.
+//   bits  0..13 start address >> 4      bits 16..29 leading byte offset >> 4
+//   bits 32..45 stride byte offset >> 4 bits 46..48 fixed 0b001
+//   bits 49..51 base offset (0: tiles are 1024-byte aligned)   bits 61..63 swizzle (2 = 128 B)
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+{
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// UMMA instruction descriptor, kind::f16: D = FP32, A = B = FP16, A K-major, B MN-major.
+//   bits 4..5 D format (1 = F32)   bits 7..9 / 10..12 A / B format (0 = F16)
+//   bit 15 A major (0 = K)          bit 16 B major (1 = MN)
+//   bits 17..22 N >> 3              bits 24..28 M >> 4
+template <int M, int N>
+__host__ __device__ constexpr uint32_t idesc_f16_f32()
+{
+    return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Grouped raster: tiles are numbered so that consecutive tile indices (which run at the
+// same time on neighbouring SMs) sweep `group_m` row-blocks of A against successive
+// column-blocks of B, keeping both operand panels hot in L2.
+__device__ __forceinline__ void tile_coords(const GemmParams &p, int t, int &mb, int &nb)
+{
+    const int per_group = p.group_m * p.n_blocks;
+    const int g = t / per_group;
+    const int first_m = g * p.group_m;
+    const int rows = min(p.m_blocks - first_m, p.group_m);
+    const int r = t - g * per_group;
+    mb = first_m + r % rows;
+    nb = r / rows;
+}
+
+struct WaitCtl {
+    volatile int *abort;   // shared-memory stop flag
+    uint32_t *err;         // device error word
+    uint64_t limit_ns;
+};
+
+// Wait for phase `parity` of `bar`; give up (and tell everyone) when the limit runs out or
+// another role has already given up.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl &w,
+                                             uint32_t code)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*w.abort)
+            return false;
+        if (global_timer_ns() - t0 > w.limit_ns) {
+            *w.abort = 1;
+            atomicCAS(w.err, 0u, code);
+            return false;
+        }
+    }
+}
+
+// Teardown wait: only the time limit (used to let in-flight copies and MMAs land).
+__device__ __forceinline__ bool wait_until(uint32_t bar, uint32_t parity, uint64_t limit_ns, uint32_t *err)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicCAS(err, 0u, static_cast<uint32_t>(ERR_TEARDOWN_DRAIN));
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ float gelu_erf(float x)
+{
+    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_b, const GemmParams p)
+{
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr uint32_t IDESC = idesc_f16_f32<BM, BN>();
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;   // swizzled tiles need 1024-byte alignment
+    uint8_t *sp = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + STAGES * Cfg::A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sp + STAGES * Cfg::STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    // barrier k lives at bar0 + 8k: full[s], empty[s], acc_full[b], acc_empty[b], drain
+    const uint32_t full0 = bar0, empty0 = bar0 + 8u * STAGES;
+    const uint32_t accf0 = bar0 + 16u * STAGES, acce0 = accf0 + 8u * Cfg::ACC_BUFS;
+    const uint32_t drain = acce0 + 8u * Cfg::ACC_BUFS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 1);
+        }
+        for (int b = 0; b < Cfg::ACC_BUFS; ++b) {
+            mbar_init(accf0 + 8u * b, 1);
+            mbar_init(acce0 + 8u * b, Cfg::NUM_EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        if (p.num_kb > 0) {
+            tma_prefetch_desc(&tmap_a);
+            tma_prefetch_desc(&tmap_b);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_parity = 0;
+            bool ok = true, withhold = (p.debug & DEBUG_WITHHOLD_FIRST_LOAD) != 0;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(p, t, mb, nb);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, wc, ERR_PRODUCER_SLOT)) {
+                        ok = false;
+                        break;
+                    }
+                    if (withhold) {
+                        withhold = false;   // test hook: this slot's operands never arrive
+                    } else {
+                        const uint32_t fb = full0 + 8u * stage;
+                        mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+                        tma_load_2d(sA + stage * Cfg::A_BYTES, &tmap_a, fb, kb * BK, mb * BM);
+#pragma unroll
+                        for (int j = 0; j < Cfg::B_BOXES; ++j)
+                            tma_load_2d(sB + stage * Cfg::B_BYTES + j * Cfg::B_BOX_BYTES, &tmap_b, fb,
+                                        nb * BN + j * Cfg::B_BOX_N, kb * BK);
+                        issued |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {   // let every copy this thread started land before the CTA exits
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued & (1u << s))
+                        wait_until(full0 + 8u * s, (issued_parity >> s) & 1u, p.timeout_ns, p.err);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                if (!wait_bounded(acce0 + 8u * acc, acc_phase ^ 1u, wc, ERR_MMA_ACCUMULATOR)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(full0 + 8u * stage, phase, wc, ERR_MMA_OPERANDS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a0 = sA + stage * Cfg::A_BYTES;
+                    const uint32_t b0 = sB + stage * Cfg::B_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk) {
+                        // A, K-major: the next 16 K-values are 32 bytes further along each
+                        // 128-byte swizzled row; 8-row groups are 1024 bytes apart.
+                        const uint64_t adesc = sw128_desc(a0 + kk * 32, 16, 1024);
+                        // B, MN-major: 16 K-rows are 2048 bytes further; 8-row K groups are
+                        // 1024 bytes apart (SBO); 64-column N atoms are one box apart (LBO).
+                        const uint64_t bdesc = sw128_desc(b0 + kk * 2048, Cfg::B_BOX_BYTES, 1024);
+                        umma_f16<1>(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(empty0 + 8u * stage);   // slot free once these MMAs have read it
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                umma_commit(accf0 + 8u * acc);          // accumulator complete
+                if (++acc == Cfg::ACC_BUFS) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (!ok) {   // let every MMA this thread issued finish before TMEM is freed
+                umma_commit(drain);
+                wait_until(drain, 0, p.timeout_ns, p.err);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue warps
+        const int quarter = warp & 3;                 // TMEM lanes this warp may access
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            int mb, nb;
+            tile_coords(p, t, mb, nb);
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_bounded(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok)
+                break;
+            tc_fence_after_sync();
+            const int row = mb * BM + quarter * 32 + lane;
+            const bool row_ok = row < p.M;
+            __half *crow = p.C + static_cast<int64_t>(row) * p.N;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                const int n0 = nb * BN + c * 32;
+                if (n0 >= p.N)
+                    break;
+                uint32_t r[32];
+                if (p.num_kb > 0) {
+                    tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c * 32), r);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        r[j] = 0u;
+                }
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[j] = __uint_as_float(r[j]);
+                if (p.bias != nullptr) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (n0 + 8 * i < p.N) {
+                            const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(p.bias + n0 + 8 * i));
+                            const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __half22float2(bh[e]);
+                                v[8 * i + 2 * e] += f.x;
+                                v[8 * i + 2 * e + 1] += f.y;
+                            }
+                        }
+                    }
+                }
+                if (p.epilogue == EPI_GELU) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = gelu_erf(v[j]);
+                } else if (p.epilogue == EPI_RELU) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = fmaxf(v[j], 0.0f);
+                }
+                if (row_ok) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (n0 + 8 * i < p.N) {
+                            uint4 out;
+                            __half2 h0 = __floats2half2_rn(v[8 * i + 0], v[8 * i + 1]);
+                            __half2 h1 = __floats2half2_rn(v[8 * i + 2], v[8 * i + 3]);
+                            __half2 h2 = __floats2half2_rn(v[8 * i + 4], v[8 * i + 5]);
+                            __half2 h3 = __floats2half2_rn(v[8 * i + 6], v[8 * i + 7]);
+                            out.x = *reinterpret_cast<uint32_t *>(&h0);
+                            out.y = *reinterpret_cast<uint32_t *>(&h1);
+                            out.z = *reinterpret_cast<uint32_t *>(&h2);
+                            out.w = *reinterpret_cast<uint32_t *>(&h3);
+                            *reinterpret_cast<uint4 *>(crow + n0 + 8 * i) = out;
+                        }
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acce0 + 8u * acc);   // this warp's rows of the accumulator are read
+            if (++acc == Cfg::ACC_BUFS) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace gb300

@@ -1,0 +1,256 @@
+"""Parity of the CUDA path (through the C ABI) with the FP64 CPU oracle, on a GB300.
+
+Inputs come from the seeded generators in ``tensor_core_gemm_tcgen05_gb300.inputs``; the
+same FP16 bits go to the device and to the oracle. The tolerance is the one in
+``tests/parity.py`` (elementwise 1e-2 + 4e-3*|ref|, relative Frobenius 1e-3, no NaN/Inf).
+Every output buffer carries guard rows and a guard tail filled with a NaN pattern, which
+must come back untouched (nothing may be written past row M-1 or column N-1).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tensor_core_gemm_tcgen05_gb300 as g
+from tensor_core_gemm_tcgen05_gb300 import inputs
+from parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 0x7E00  # an FP16 NaN
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    from tensor_core_gemm_tcgen05_gb300 import _build
+    _build.build()
+    c = g.Context(0)
+    yield c
+    c.close()
+
+
+def run_guarded(ctx, A, B, bias, epi, stream=None):
+    """Run the GEMM into a buffer with 3 guard rows and a 40-element guard tail; check the
+    guards and return the M x N result on the host."""
+    M, K = A.shape
+    N = B.shape[1]
+    dev = torch.device("cuda:0")
+    buf = torch.full(((M + 3) * N + 40,), GUARD, dtype=torch.int16, device=dev)
+    Cv = buf[: M * N].view(torch.float16).view(M, N)
+    dA, dB = A.to(dev), B.to(dev)
+    dbias = bias.to(dev) if bias is not None else None
+    g.gemm(ctx, dA, dB, dbias, epi, out=Cv, stream=stream)
+    torch.cuda.synchronize()
+    assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+    tail = buf[M * N:].cpu()
+    assert torch.all(tail == GUARD), "kernel wrote past the end of C"
+    return Cv.cpu()
+
+
+def oracle_ref(A, B, bias, epi, rows=None):
+    ref, _, _ = oracle.gemm(A, B, bias, epi, rows=rows)
+    return ref
+
+
+def check(ctx, M, N, K, epi=g.EPI_NONE, with_bias=False, seed=0, dist="uniform"):
+    A = inputs.random_fp16((M, K), 1000 + seed, dist, k=K)
+    B = inputs.random_fp16((K, N), 2000 + seed, dist, k=K)
+    bias = inputs.random_fp16((N,), 3000 + seed) if with_bias else None
+    C = run_guarded(ctx, A, B, bias, epi)
+    return assert_parity(C.numpy(), oracle_ref(A, B, bias, epi), f"M={M} N={N} K={K} epi={epi}")
+
+
+# ---- one tile first: pins the UMMA descriptors, TMEM layout and the mbarrier ring ---------
+
+def test_single_tile_single_kblock(ctx):
+    check(ctx, 128, 256, 64)
+
+
+def test_single_tile_identity(ctx):
+    # A = I (128 x 128) selects B's rows exactly: any descriptor or layout slip shows.
+    K = 128
+    A = torch.eye(128, K, dtype=torch.float16)
+    B = inputs.random_fp16((K, 256), 5)
+    C = run_guarded(ctx, A, B, None, g.EPI_NONE)
+    assert torch.equal(C, B)
+    # B = I picks A
+    A2 = inputs.random_fp16((128, 256), 6)
+    C2 = run_guarded(ctx, A2, torch.eye(256, dtype=torch.float16), None, g.EPI_NONE)
+    assert torch.equal(C2, A2)
+
+
+def test_all_ones_gives_k(ctx):
+    for K in (64, 2048):
+        A = torch.ones(130, K, dtype=torch.float16)
+        B = torch.ones(K, 264, dtype=torch.float16)
+        C = run_guarded(ctx, A, B, None, g.EPI_NONE)
+        assert torch.all(C == K)
+
+
+# ---- ragged shapes, every epilogue -----------------------------------------------------------
+
+SHAPES = [
+    (128, 256, 128), (1, 256, 64), (8, 256, 128), (127, 256, 192), (129, 512, 64),
+    (255, 768, 256), (256, 256, 512), (257, 512, 320), (300, 264, 200), (64, 8, 8),
+    (200, 72, 40), (1000, 1000, 1000), (77, 320, 4096),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_ragged_shapes_plain(ctx, shape):
+    check(ctx, *shape, seed=sum(shape))
+
+
+@pytest.mark.parametrize("epi,with_bias", [(g.EPI_NONE, True), (g.EPI_GELU, True), (g.EPI_RELU, True),
+                                           (g.EPI_GELU, False), (g.EPI_RELU, False)])
+@pytest.mark.parametrize("shape", [(129, 264, 200), (300, 512, 1024), (8, 2048, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_epilogues(ctx, shape, epi, with_bias):
+    check(ctx, *shape, epi=epi, with_bias=with_bias, seed=shape[0] + 7 * epi)
+
+
+def test_more_tiles_than_sms(ctx):
+    # 16 x 10 = 160 tiles of 128 x 256 on ~150 SMs, then 32 x 16 = 512 tiles: every CTA
+    # runs several tiles, both TMEM accumulators and many ring phases.
+    check(ctx, 2048, 2560, 256, epi=g.EPI_GELU, with_bias=True, seed=1)
+    check(ctx, 4096, 4096, 128, epi=g.EPI_RELU, with_bias=True, seed=2)
+
+
+def test_k_zero_gives_activation_of_bias(ctx):
+    M, N = 70, 264
+    bias = inputs.random_fp16((N,), 9)
+    dev = torch.device("cuda:0")
+    for epi in (g.EPI_NONE, g.EPI_GELU, g.EPI_RELU):
+        C = torch.empty(M, N, dtype=torch.float16, device=dev)
+        g.gemm_run(ctx, M, N, 0, None, None, bias.to(dev), C, epi)
+        torch.cuda.synchronize()
+        ref = oracle_ref(torch.zeros(M, 0, dtype=torch.float16), torch.zeros(0, N, dtype=torch.float16),
+                         bias, epi)
+        assert_parity(C.cpu().numpy(), ref, f"K=0 epi={epi}")
+
+
+def test_empty_m_or_n_is_a_no_op(ctx):
+    dev = torch.device("cuda:0")
+    C = torch.full((4, 8), 3.0, dtype=torch.float16, device=dev)
+    A = torch.ones(4, 8, dtype=torch.float16, device=dev)
+    B = torch.ones(8, 8, dtype=torch.float16, device=dev)
+    assert g.gemm_run(ctx, 0, 8, 8, A, B, None, C) == g.GEMM_OK
+    assert g.gemm_run(ctx, 4, 0, 8, A, B, None, C) == g.GEMM_OK
+    torch.cuda.synchronize()
+    assert torch.all(C == 3.0)
+
+
+# ---- the benchmark problems --------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", list(inputs.WORKLOADS))
+def test_workload_parity(ctx, name):
+    w = inputs.WORKLOADS[name]
+    A, B, bias = inputs.make_inputs(w)
+    rows = inputs.sample_rows(w.M, w.sample_rows, include_last=w.include_last)
+    dev = torch.device("cuda:0")
+    C = torch.empty(w.M, w.N, dtype=torch.float16, device=dev)
+    g.gemm(ctx, A.to(dev), B.to(dev), None if bias is None else bias.to(dev), w.epi_code, out=C)
+    torch.cuda.synchronize()
+    assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+    got = C[rows.to(dev)].cpu().numpy()
+    ref = oracle_ref(A, B, bias, w.epi_code, rows=rows.numpy())
+    s = assert_parity(got, ref, name)
+    if w.sample_rows:
+        # properties that hold at any size, over the whole output
+        assert bool(torch.isfinite(C).all())
+        if w.epilogue == "gelu":
+            assert float(C.min()) >= -0.1701 - 1e-3   # GELU is bounded below by about -0.17
+
+
+# ---- boundary behaviour on the device --------------------------------------------------------------
+
+def test_bad_arguments_are_rejected_before_launch(ctx):
+    dev = torch.device("cuda:0")
+    A = torch.zeros(64, 64, dtype=torch.float16, device=dev)
+    B = torch.zeros(64, 64, dtype=torch.float16, device=dev)
+    C = torch.zeros(64, 64, dtype=torch.float16, device=dev)
+    L, h = g.lib(), ctx.handle
+
+    def rc(M=64, N=64, K=64, a=A.data_ptr(), b=B.data_ptr(), bias=None, c=C.data_ptr(), epi=0):
+        return L.gemm_run(h, M, N, K, a, b, bias, c, epi, None)
+
+    assert rc() == g.GEMM_OK
+    assert rc(M=-1) == g.GEMM_ERR_ARG
+    assert rc(K=2 ** 31) == g.GEMM_ERR_ARG
+    assert rc(epi=3) == g.GEMM_ERR_ARG
+    assert rc(a=None) == g.GEMM_ERR_ARG
+    assert rc(c=None) == g.GEMM_ERR_ARG
+    assert rc(N=60) == g.GEMM_ERR_ALIGN
+    assert rc(K=36) == g.GEMM_ERR_ALIGN
+    assert rc(a=A.data_ptr() + 2) == g.GEMM_ERR_ALIGN
+    assert rc(bias=C.data_ptr() + 8) == g.GEMM_ERR_ALIGN
+    assert rc(c=A.data_ptr()) == g.GEMM_ERR_ARG                        # C overlaps A
+    host = np.zeros(64 * 64 + 8, dtype=np.float16)
+    hp = (host.ctypes.data + 15) // 16 * 16
+    assert rc(a=hp) == g.GEMM_ERR_DEVICE                                # host memory
+    assert rc(c=hp) == g.GEMM_ERR_DEVICE
+    torch.cuda.synchronize()
+    assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+    assert g.gemm_num_sms(ctx) >= 100
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(ctx):
+    """The producer withholds its first operand load, so the MMA warp's wait runs out:
+    the kernel must return (no hang, no fault) and report GEMM_ERR_TIMEOUT; afterwards the
+    same context computes correct results again."""
+    g.gemm_set_timeout_ns(ctx, 20_000_000)
+    g.gemm_set_debug(ctx, g.GEMM_DEBUG_WITHHOLD_FIRST_LOAD)
+    try:
+        dev = torch.device("cuda:0")
+        A = torch.ones(128, 64, dtype=torch.float16, device=dev)
+        B = torch.ones(64, 256, dtype=torch.float16, device=dev)
+        C = torch.zeros(128, 256, dtype=torch.float16, device=dev)
+        g.gemm(ctx, A, B, None, g.EPI_NONE, out=C)
+        torch.cuda.synchronize()
+        status, detail = g.gemm_last_device_error(ctx)
+        assert status == g.GEMM_ERR_TIMEOUT
+        assert detail in (1, 2, 3, 4, 5)
+        assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)   # cleared
+    finally:
+        g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
+        g.gemm_set_timeout_ns(ctx, 2_000_000_000)
+    check(ctx, 256, 512, 256, epi=g.EPI_GELU, with_bias=True, seed=3)
+
+
+def test_host_buffer_entry_point(ctx):
+    M, N, K = 300, 512, 256
+    A = inputs.random_fp16((M, K), 71).pin_memory()
+    B = inputs.random_fp16((K, N), 72).pin_memory()
+    bias = inputs.random_fp16((N,), 73).pin_memory()
+    C = torch.empty(M, N, dtype=torch.float16).pin_memory()
+    g.gemm_run_host(ctx, M, N, K, A, B, bias, C, g.EPI_GELU)
+    assert_parity(C.numpy(), oracle_ref(A, B, bias, g.EPI_GELU), "gemm_run_host")
+    # pageable memory works too
+    C2 = torch.empty(M, N, dtype=torch.float16)
+    g.gemm_run_host(ctx, M, N, K, A.clone(), B.clone(), None, C2, g.EPI_RELU)
+    assert_parity(C2.numpy(), oracle_ref(A, B, None, g.EPI_RELU), "gemm_run_host pageable")
+
+
+def test_side_stream_and_cuda_graph(ctx):
+    dev = torch.device("cuda:0")
+    M, N, K = 640, 768, 512
+    A = inputs.random_fp16((M, K), 81)
+    B = inputs.random_fp16((K, N), 82)
+    bias = inputs.random_fp16((N,), 83)
+    dA, dB, dbias = A.to(dev), B.to(dev), bias.to(dev)
+    ref = oracle_ref(A, B, bias, g.EPI_GELU)
+    s = torch.cuda.Stream()
+    C = torch.empty(M, N, dtype=torch.float16, device=dev)
+    with torch.cuda.stream(s):
+        g.gemm(ctx, dA, dB, dbias, g.EPI_GELU, out=C)
+    s.synchronize()
+    assert_parity(C.cpu().numpy(), ref, "side stream")
+    C.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.gemm(ctx, dA, dB, dbias, g.EPI_GELU, out=C)
+    for _ in range(3):
+        C.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    assert_parity(C.cpu().numpy(), ref, "graph replay")
