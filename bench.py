@@ -253,7 +253,7 @@ def measure_e2e(g, ctx, w, host, stream, steps):
             "ms_per_step": round(dt * 1e3 / steps, 4), "api": "gemm_run_host (pinned host buffers)"}
 
 
-def cpu_baseline(w, host, target_s=12.0, max_rows=512):
+def cpu_baseline(w, host, target_s=12.0, max_rows=None):
     """The FP64 oracle, as it stands, on a bounded row sample of the workload."""
     import oracle
     from tensor_core_gemm_tcgen05_gb300 import inputs
@@ -264,7 +264,7 @@ def cpu_baseline(w, host, target_s=12.0, max_rows=512):
     _, _, used = oracle.gemm(A, B, bias, w.epi_code, rows=probe_rows)
     t_probe = time.perf_counter() - t0
     rate = len(probe_rows) / max(t_probe, 1e-6)
-    nrows = int(min(max_rows, max(len(probe_rows), rate * target_s)))
+    nrows = int(min(max_rows or w.M, max(len(probe_rows), rate * target_s)))
     rows = inputs.sample_rows(w.M, nrows, include_last=min(w.include_last, nrows)).numpy()
     t0 = time.perf_counter()
     _, _, used = oracle.gemm(A, B, bias, w.epi_code, rows=rows)
