@@ -126,6 +126,35 @@ enum { GEMM_DEBUG_NONE = 0, GEMM_DEBUG_WITHHOLD_FIRST_LOAD = 1 };
 int gemm_set_timeout_ns(gemm_ctx *ctx, uint64_t ns);
 int gemm_set_debug(gemm_ctx *ctx, int flags);
 
+/* ---- Allocation-free variant ----------------------------------------------------------
+ * The tutorial pages have no counterpart to this call; it exists for callers that cannot
+ * allocate device memory. gemm_create allocates the kernel's scratch (a 4-byte device
+ * error word) with cudaMalloc, which some callers may not do: plugins of an inference
+ * engine that owns all device memory, real-time loops that forbid allocation after
+ * start-up, code running where the allocator must not be touched.
+ *
+ * gemm_run_noalloc computes the same C = act(A*B + bias) with the same kernel and the
+ * same argument rules as gemm_run (device pointers on the CURRENT device, N and K multiples
+ * of 8, 16-byte alignment, M, N, K <= 2^31 - 1; larger sizes return GEMM_ERR_ARG), but
+ * needs no context and calls no cudaMalloc, cudaFree or allocating library routine.
+ * Its scratch is a file-scope __device__ array of GEMM_NOALLOC_SCRATCH_BYTES bytes that
+ * every GPU loading the library holds until the process exits; this kernel needs 4 bytes
+ * of it (the error word) whatever the problem size.
+ *  - The first call on a device does a one-time set-up there (checks the device, sets
+ *    the kernel's shared-memory limit, resolves the tensor-map encoder, looks up the
+ *    array's device address). Make that first call before any stream capture.
+ *  - Every call on a device shares the one array and clears the error word on `stream`
+ *    before its launch. Calls whose kernels overlap on the GPU (different streams) race
+ *    on the error word.
+ *  - An in-kernel wait that runs out still ends the kernel cleanly, but this call has no
+ *    way to report it (it returns before the kernel runs); use gemm_run and
+ *    gemm_last_device_error where that report is needed.
+ * Returns GEMM_OK once the work is enqueued, or an error code before anything is enqueued
+ * (GEMM_ERR_LAUNCH if the launch itself fails). */
+#define GEMM_NOALLOC_SCRATCH_BYTES 256
+int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+                     const void *bias, void *C, int epilogue, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

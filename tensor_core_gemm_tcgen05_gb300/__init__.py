@@ -39,8 +39,9 @@ GEMM_DEBUG_WITHHOLD_FIRST_LOAD = 1
 EXPORTS = (
     "gemm_create", "gemm_run", "gemm_run_host", "gemm_last_device_error",
     "gemm_last_cuda_error", "gemm_destroy", "gemm_status_string", "gemm_num_sms",
-    "gemm_set_timeout_ns", "gemm_set_debug",
+    "gemm_set_timeout_ns", "gemm_set_debug", "gemm_run_noalloc",
 )
+GEMM_NOALLOC_SCRATCH_BYTES = 256
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +78,7 @@ def lib() -> ctypes.CDLL:
             L.gemm_num_sms.argtypes = [vp]
             L.gemm_set_timeout_ns.argtypes = [vp, ctypes.c_uint64]
             L.gemm_set_debug.argtypes = [vp, i32]
+            L.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, i32, vp]
             for name in EXPORTS:
                 if name != "gemm_status_string":
                     getattr(L, name).restype = i32
@@ -159,6 +161,13 @@ def gemm_run_host(ctx, M, N, K, A, B, bias, C, epilogue=EPI_NONE, stream=None) -
     rc = lib().gemm_run_host(_h(ctx), M, N, K, _ptr(A), _ptr(B), _ptr(bias), _ptr(C), int(epilogue),
                              _stream(stream, _dev(ctx)))
     return _check(rc, "gemm_run_host")
+
+
+def gemm_run_noalloc(M, N, K, A, B, bias, C, epilogue=EPI_NONE, stream=None, device=None) -> int:
+    """The allocation-free variant (no context; device pointers on the current device)."""
+    rc = lib().gemm_run_noalloc(M, N, K, _ptr(A), _ptr(B), _ptr(bias), _ptr(C), int(epilogue),
+                                _stream(stream, device))
+    return _check(rc, "gemm_run_noalloc")
 
 
 def gemm_last_device_error(ctx) -> tuple[int, int]:

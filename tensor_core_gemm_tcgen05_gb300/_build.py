@@ -9,7 +9,7 @@ import subprocess
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libgb300gemm.so")
-SOURCES = [os.path.join(PKG, "csrc", "gemm_api.cu")]
+SOURCES = [os.path.join(PKG, "csrc", "gemm_api.cu"), os.path.join(PKG, "csrc", "gemm_noalloc.cu")]
 DEPS = SOURCES + glob.glob(os.path.join(PKG, "csrc", "*.cuh")) + [os.path.join(ROOT, "include", "gemm.h")]
 
 NVCC_FLAGS = [
