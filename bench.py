@@ -358,7 +358,7 @@ def run_ours(args):
             del a, b, bi, c
         torch.cuda.empty_cache()
 
-    e2e = measure_e2e(g, ctx, w, host, stream, steps=max(3, min(args.steps, 10)))
+    e2e = None if args.no_e2e else measure_e2e(g, ctx, w, host, stream, steps=max(3, min(args.steps, 10)))
     base = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, host)
     ctx.close()
 
@@ -440,6 +440,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-side", action="store_true", help="skip the context workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -113,16 +113,31 @@ int gemm_destroy(gemm_ctx *ctx);
 /* A static, human-readable name for a status code. */
 const char *gemm_status_string(int status);
 
-/* Number of streaming multiprocessors the persistent kernel sizes its grid to. */
+/* Number of streaming multiprocessors the one-CTA kernel sizes its grid to. */
 int gemm_num_sms(gemm_ctx *ctx);
 
-/* Test hooks for the failure path (no effect on results when left at their defaults).
+/* Number of CTA pairs (2-SM clusters) the device can run at once with the pair kernel,
+ * which takes 256 x 256 tiles; 0 if the pair kernel cannot run (then every call uses the
+ * one-CTA kernel). gemm_run picks the pair kernel when the problem has at least this many
+ * 256 x 256 tiles, else the one-CTA kernel (128 x 256 tiles). */
+int gemm_num_pairs(gemm_ctx *ctx);
+
+/* Test hooks (no effect on results when left at their defaults).
  *   gemm_set_timeout_ns: the limit of every in-kernel wait (default 2e9 ns; values below
  *     1e6 are raised to 1e6).
- *   gemm_set_debug: GEMM_DEBUG_WITHHOLD_FIRST_LOAD makes the producer of every CTA hold
- *     back its first operand load, so that the MMA's wait on it runs out and the kernel
- *     must take its timeout path (a flag that nothing sets; no fault, no hang). */
-enum { GEMM_DEBUG_NONE = 0, GEMM_DEBUG_WITHHOLD_FIRST_LOAD = 1 };
+ *   gemm_set_debug, a bitwise OR of:
+ *     GEMM_DEBUG_WITHHOLD_FIRST_LOAD: the producer (of CTA 0 of each pair, or of every
+ *       CTA) holds back its first operand load, so that the MMA's wait on it runs out and
+ *       the kernel must take its timeout path (a flag that nothing sets; no fault, no hang);
+ *     GEMM_DEBUG_FORCE_SINGLE / GEMM_DEBUG_FORCE_PAIR: override the kernel choice, so that
+ *       tests can run any shape through either kernel (FORCE_PAIR is ignored when the
+ *       pair kernel cannot run). */
+enum {
+    GEMM_DEBUG_NONE = 0,
+    GEMM_DEBUG_WITHHOLD_FIRST_LOAD = 1,
+    GEMM_DEBUG_FORCE_SINGLE = 2,
+    GEMM_DEBUG_FORCE_PAIR = 4
+};
 int gemm_set_timeout_ns(gemm_ctx *ctx, uint64_t ns);
 int gemm_set_debug(gemm_ctx *ctx, int flags);
 

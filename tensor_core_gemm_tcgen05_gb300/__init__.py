@@ -34,12 +34,14 @@ GEMM_ERR_TIMEOUT = -5
 GEMM_ERR_NOMEM = -6
 GEMM_DEBUG_NONE = 0
 GEMM_DEBUG_WITHHOLD_FIRST_LOAD = 1
+GEMM_DEBUG_FORCE_SINGLE = 2
+GEMM_DEBUG_FORCE_PAIR = 4
 
 # Every symbol include/gemm.h declares (the CPU tests check the library exports them).
 EXPORTS = (
     "gemm_create", "gemm_run", "gemm_run_host", "gemm_last_device_error",
     "gemm_last_cuda_error", "gemm_destroy", "gemm_status_string", "gemm_num_sms",
-    "gemm_set_timeout_ns", "gemm_set_debug", "gemm_run_noalloc",
+    "gemm_set_timeout_ns", "gemm_set_debug", "gemm_run_noalloc", "gemm_num_pairs",
 )
 GEMM_NOALLOC_SCRATCH_BYTES = 256
 
@@ -76,6 +78,7 @@ def lib() -> ctypes.CDLL:
             L.gemm_status_string.argtypes = [i32]
             L.gemm_status_string.restype = ctypes.c_char_p
             L.gemm_num_sms.argtypes = [vp]
+            L.gemm_num_pairs.argtypes = [vp]
             L.gemm_set_timeout_ns.argtypes = [vp, ctypes.c_uint64]
             L.gemm_set_debug.argtypes = [vp, i32]
             L.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, i32, vp]
@@ -193,6 +196,10 @@ def gemm_status_string(status: int) -> str:
 
 def gemm_num_sms(ctx) -> int:
     return int(lib().gemm_num_sms(_h(ctx)))
+
+
+def gemm_num_pairs(ctx) -> int:
+    return int(lib().gemm_num_pairs(_h(ctx)))
 
 
 def gemm_set_timeout_ns(ctx, ns: int) -> int:

@@ -11,11 +11,36 @@
 
 #include "gemm.h"
 #include "gemm_kernel.cuh"
+#include "gemm_kernel_pair.cuh"
 
 namespace {
 
-using Cfg = gb300::KernelConfig<128, 256, 4>;
+#ifndef GB300_EPI_WARPS
+#define GB300_EPI_WARPS 4
+#endif
+using Cfg = gb300::KernelConfig<128, 256, 4, GB300_EPI_WARPS>;
+#ifndef GB300_PAIR_STAGES
+#define GB300_PAIR_STAGES 6
+#endif
+using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS>;
 constexpr int kGroupM = 16;
+#ifndef GB300_PAIR_GROUP_M
+#define GB300_PAIR_GROUP_M 8
+#endif
+constexpr int kPairGroupM = GB300_PAIR_GROUP_M;
+#ifndef GB300_L2_RESIDENT_MB
+#define GB300_L2_RESIDENT_MB 0
+#endif
+// When A is at most this large, the raster sweeps all row blocks for each column band so
+// that B streams through L2 once while A stays resident (0 disables the rule).
+constexpr int64_t kL2ResidentBytes = static_cast<int64_t>(GB300_L2_RESIDENT_MB) << 20;
+
+int raster_group(int m_blocks, int64_t a_bytes, int default_group)
+{
+    if (kL2ResidentBytes > 0 && a_bytes <= kL2ResidentBytes)
+        return m_blocks;
+    return default_group;
+}
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr uint64_t kMinTimeoutNs = 1000000ull;
 
@@ -29,6 +54,7 @@ struct gemm_ctx {
     uint64_t timeout_ns = kDefaultTimeoutNs;
     int debug = 0;
     int last_cuda_error = 0;
+    int max_clusters = 0;   // co-resident CTA pairs of the pair kernel (0: pair kernel unusable)
     // staging buffers of gemm_run_host
     void *stage = nullptr;
     size_t stage_bytes = 0;
@@ -145,19 +171,36 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     p.M = M;
     p.N = N;
     p.K = K;
-    p.m_blocks = (M + Cfg::BM - 1) / Cfg::BM;
-    p.n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
-    p.num_tiles = p.m_blocks * p.n_blocks;
     p.num_kb = (K + Cfg::BK - 1) / Cfg::BK;
-    p.group_m = kGroupM;
     p.epilogue = epilogue;
     p.bias = static_cast<const __half *>(bias);
     p.C = static_cast<__half *>(C);
     p.err = ctx->d_err;
     p.timeout_ns = ctx->timeout_ns;
-    p.debug = ctx->debug;
-    const int grid = std::min(p.num_tiles, ctx->num_sms);
-    gb300::gemm_tcgen05_kernel<Cfg><<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, p);
+    p.debug = ctx->debug & GEMM_DEBUG_WITHHOLD_FIRST_LOAD;
+    // 256 x 256 tiles on CTA pairs when there are enough of them to give every pair at
+    // least one; otherwise 128 x 256 tiles on single SMs (twice as many tiles to spread).
+    const int pair_tiles = ((M + PairCfg::BM - 1) / PairCfg::BM) * ((N + PairCfg::BN - 1) / PairCfg::BN);
+    bool pair = ctx->max_clusters > 0 && pair_tiles >= ctx->max_clusters;
+    if (ctx->debug & GEMM_DEBUG_FORCE_SINGLE)
+        pair = false;
+    if ((ctx->debug & GEMM_DEBUG_FORCE_PAIR) && ctx->max_clusters > 0)
+        pair = true;
+    if (pair) {
+        p.m_blocks = (M + PairCfg::BM - 1) / PairCfg::BM;
+        p.n_blocks = (N + PairCfg::BN - 1) / PairCfg::BN;
+        p.num_tiles = p.m_blocks * p.n_blocks;
+        p.group_m = raster_group(p.m_blocks, static_cast<int64_t>(M) * K * 2, kPairGroupM);
+        const int grid = 2 * std::min(p.num_tiles, ctx->max_clusters);
+        gb300::gemm_tcgen05_pair_kernel<PairCfg><<<grid, PairCfg::NUM_THREADS, PairCfg::SMEM_BYTES, stream>>>(ta, tb, p);
+    } else {
+        p.m_blocks = (M + Cfg::BM - 1) / Cfg::BM;
+        p.n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
+        p.num_tiles = p.m_blocks * p.n_blocks;
+        p.group_m = raster_group(p.m_blocks, static_cast<int64_t>(M) * K * 2, kGroupM);
+        const int grid = std::min(p.num_tiles, ctx->num_sms);
+        gb300::gemm_tcgen05_kernel<Cfg><<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, p);
+    }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
@@ -200,6 +243,18 @@ int gemm_create(gemm_ctx **out, int device)
         delete ctx;
         return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);
     }
+    // The pair kernel is used only if the device can co-schedule its clusters.
+    if (cudaFuncSetAttribute(gb300::gemm_tcgen05_pair_kernel<PairCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PairCfg::SMEM_BYTES) == cudaSuccess) {
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(2 * (sms / 2), 1, 1);
+        lc.blockDim = dim3(PairCfg::NUM_THREADS, 1, 1);
+        lc.dynamicSmemBytes = PairCfg::SMEM_BYTES;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, gb300::gemm_tcgen05_pair_kernel<PairCfg>, &lc) == cudaSuccess)
+            ctx->max_clusters = clusters;
+    }
+    cudaGetLastError();
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
@@ -333,6 +388,8 @@ const char *gemm_status_string(int status)
 
 int gemm_num_sms(gemm_ctx *ctx) { return ctx ? ctx->num_sms : 0; }
 
+int gemm_num_pairs(gemm_ctx *ctx) { return ctx ? ctx->max_clusters : 0; }
+
 int gemm_set_timeout_ns(gemm_ctx *ctx, uint64_t ns)
 {
     if (!ctx)
@@ -343,7 +400,7 @@ int gemm_set_timeout_ns(gemm_ctx *ctx, uint64_t ns)
 
 int gemm_set_debug(gemm_ctx *ctx, int flags)
 {
-    if (!ctx || (flags & ~GEMM_DEBUG_WITHHOLD_FIRST_LOAD))
+    if (!ctx || (flags & ~(GEMM_DEBUG_WITHHOLD_FIRST_LOAD | GEMM_DEBUG_FORCE_SINGLE | GEMM_DEBUG_FORCE_PAIR)))
         return GEMM_ERR_ARG;
     ctx->debug = flags;
     return GEMM_OK;

@@ -16,9 +16,11 @@
 //  * warp 1: allocates Tensor Memory and issues tcgen05.mma (M = BM, N = BN, K = 16) from
 //    one thread into one of two FP32 TMEM accumulators, releasing each slot with
 //    tcgen05.commit;
-//  * warps 2..5: epilogue. Each warp owns one 32-lane quarter of TMEM (= 32 rows of the
-//    tile); it reads its rows with tcgen05.ld, adds the bias, applies the activation in
-//    FP32, rounds to FP16 and writes 16-byte vectors, masking rows >= M and columns >= N.
+//  * warps 2..(1+EPI_WARPS): epilogue. A warp may only read the 32-lane quarter of TMEM
+//    given by its warp index mod 4 (= 32 rows of the tile); with 4 epilogue warps each
+//    takes all BN columns of its quarter, with 8 each takes half of them. A warp reads its
+//    rows with tcgen05.ld, adds the bias, applies the activation in FP32, rounds to FP16
+//    and writes 16-byte vectors, masking rows >= M and columns >= N.
 //    While it drains accumulator b, the MMA warp already fills accumulator b ^ 1.
 //
 // Every mbarrier wait is bounded in time. When a wait runs out the kernel records which
@@ -59,7 +61,7 @@ struct GemmParams {
     int debug;             // DEBUG_* flags
 };
 
-template <int BM_, int BN_, int STAGES_>
+template <int BM_, int BN_, int STAGES_, int EPI_WARPS_ = 4>
 struct KernelConfig {
     static constexpr int BM = BM_;          // rows of A / C per tile (= UMMA M, = TMEM lanes)
     static constexpr int BN = BN_;          // columns of B / C per tile (= UMMA N)
@@ -74,7 +76,8 @@ struct KernelConfig {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int ACC_BUFS = 2;
     static constexpr int TMEM_COLS = ACC_BUFS * BN;    // FP32 accumulators, one column each
-    static constexpr int NUM_EPI_WARPS = 4;
+    static constexpr int NUM_EPI_WARPS = EPI_WARPS_;
+    static constexpr int EPI_COL_GROUPS = NUM_EPI_WARPS / 4;   // warps sharing a TMEM quarter
     static constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES +
@@ -83,6 +86,8 @@ struct KernelConfig {
     static_assert(BM == 128, "one CTA, M = 128: TMEM lane i holds tile row i");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM alloc size");
+    static_assert(NUM_EPI_WARPS == 4 || NUM_EPI_WARPS == 8, "one or two warps per TMEM lane quarter");
+    static_assert((BN / 32) % EPI_COL_GROUPS == 0, "column chunks split evenly between warps");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 };
 
@@ -162,9 +167,95 @@ __device__ __forceinline__ bool wait_until(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
+#ifndef GB300_GELU_AS7126
+#define GB300_GELU_AS7126 0
+#endif
+
+#if GB300_GELU_AS7126
+// GELU(x) = x * Phi(x), Phi(x) = 1 - erfc(x / sqrt(2)) / 2 for x >= 0 and erfc(|x| / sqrt(2)) / 2
+// for x < 0. erfc(z), z >= 0, from Abramowitz & Stegun, Handbook of Mathematical Functions,
+// formula 7.1.26 (Hastings): erfc(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
+// t = 1 / (1 + p z), absolute error <= 1.5e-7. Branch-free; no cancellation for x < 0.
+__device__ __forceinline__ float gelu_erf(float x)
+{
+    const float z = fabsf(x) * 0.70710678118654752f;
+    const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
+    float poly = fmaf(t, 1.061405429f, -1.453152027f);
+    poly = fmaf(t, poly, 1.421413741f);
+    poly = fmaf(t, poly, -0.284496736f);
+    poly = fmaf(t, poly, 0.254829592f);
+    const float erfc_z = poly * t * __expf(-z * z);
+    const float phi = x >= 0.0f ? fmaf(-0.5f, erfc_z, 1.0f) : 0.5f * erfc_z;
+    return x * phi;
+}
+#else
 __device__ __forceinline__ float gelu_erf(float x)
 {
     return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+#endif
+
+// One 32-column chunk of one accumulator row per thread: TMEM -> registers (tcgen05.ld),
+// + bias, activation, FP32 -> FP16 (round to nearest even), four 16-byte stores.
+// Called by all 32 lanes of an epilogue warp together (tcgen05.ld is warp-collective);
+// `row_ok` masks rows >= M, and column groups of 8 at or past N are skipped.
+__device__ __forceinline__ void epilogue_chunk(const GemmParams &p, uint32_t taddr, int n0, __half *crow,
+                                               bool row_ok)
+{
+    uint32_t r[32];
+    if (p.num_kb > 0) {
+        tmem_ld_32x32b_x32(taddr, r);
+        tmem_ld_wait();
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            r[j] = 0u;   // K = 0: the empty sum
+    }
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        v[j] = __uint_as_float(r[j]);
+    if (p.bias != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (n0 + 8 * i < p.N) {
+                const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(p.bias + n0 + 8 * i));
+                const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(bh[e]);
+                    v[8 * i + 2 * e] += f.x;
+                    v[8 * i + 2 * e + 1] += f.y;
+                }
+            }
+        }
+    }
+    if (p.epilogue == EPI_GELU) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            v[j] = gelu_erf(v[j]);
+    } else if (p.epilogue == EPI_RELU) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            v[j] = fmaxf(v[j], 0.0f);
+    }
+    if (row_ok) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (n0 + 8 * i < p.N) {
+                uint4 out;
+                __half2 h0 = __floats2half2_rn(v[8 * i + 0], v[8 * i + 1]);
+                __half2 h1 = __floats2half2_rn(v[8 * i + 2], v[8 * i + 3]);
+                __half2 h2 = __floats2half2_rn(v[8 * i + 4], v[8 * i + 5]);
+                __half2 h3 = __floats2half2_rn(v[8 * i + 6], v[8 * i + 7]);
+                out.x = *reinterpret_cast<uint32_t *>(&h0);
+                out.y = *reinterpret_cast<uint32_t *>(&h1);
+                out.z = *reinterpret_cast<uint32_t *>(&h2);
+                out.w = *reinterpret_cast<uint32_t *>(&h3);
+                *reinterpret_cast<uint4 *>(crow + n0 + 8 * i) = out;
+            }
+        }
+    }
 }
 
 template <class Cfg>
@@ -315,6 +406,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         // ------------------------------------------------------------ epilogue warps
         const int quarter = warp & 3;                 // TMEM lanes this warp may access
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        constexpr int CHUNKS = BN / 32 / Cfg::EPI_COL_GROUPS;   // 32-column chunks per warp
+        const int c_begin = ((warp - 2) >> 2) * CHUNKS;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
@@ -331,64 +424,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const bool row_ok = row < p.M;
             __half *crow = p.C + static_cast<int64_t>(row) * p.N;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = c_begin; c < c_begin + CHUNKS; ++c) {
                 const int n0 = nb * BN + c * 32;
                 if (n0 >= p.N)
                     break;
-                uint32_t r[32];
-                if (p.num_kb > 0) {
-                    tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c * 32), r);
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        r[j] = 0u;
-                }
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    v[j] = __uint_as_float(r[j]);
-                if (p.bias != nullptr) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if (n0 + 8 * i < p.N) {
-                            const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(p.bias + n0 + 8 * i));
-                            const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = __half22float2(bh[e]);
-                                v[8 * i + 2 * e] += f.x;
-                                v[8 * i + 2 * e + 1] += f.y;
-                            }
-                        }
-                    }
-                }
-                if (p.epilogue == EPI_GELU) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = gelu_erf(v[j]);
-                } else if (p.epilogue == EPI_RELU) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = fmaxf(v[j], 0.0f);
-                }
-                if (row_ok) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if (n0 + 8 * i < p.N) {
-                            uint4 out;
-                            __half2 h0 = __floats2half2_rn(v[8 * i + 0], v[8 * i + 1]);
-                            __half2 h1 = __floats2half2_rn(v[8 * i + 2], v[8 * i + 3]);
-                            __half2 h2 = __floats2half2_rn(v[8 * i + 4], v[8 * i + 5]);
-                            __half2 h3 = __floats2half2_rn(v[8 * i + 6], v[8 * i + 7]);
-                            out.x = *reinterpret_cast<uint32_t *>(&h0);
-                            out.y = *reinterpret_cast<uint32_t *>(&h1);
-                            out.z = *reinterpret_cast<uint32_t *>(&h2);
-                            out.w = *reinterpret_cast<uint32_t *>(&h3);
-                            *reinterpret_cast<uint4 *>(crow + n0 + 8 * i) = out;
-                        }
-                    }
-                }
+                epilogue_chunk(p, tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c * 32), n0, crow, row_ok);
             }
             tc_fence_before_sync();
             __syncwarp();

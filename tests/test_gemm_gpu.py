@@ -29,6 +29,17 @@ def ctx():
     c.close()
 
 
+@pytest.fixture(params=["single", "pair"])
+def kctx(ctx, request):
+    """The context with the kernel choice forced: one-CTA 128x256 tiles or CTA-pair
+    256x256 tiles (cta_group::2)."""
+    if request.param == "pair" and g.gemm_num_pairs(ctx) == 0:
+        pytest.skip("the pair kernel cannot run on this device")
+    g.gemm_set_debug(ctx, g.GEMM_DEBUG_FORCE_SINGLE if request.param == "single" else g.GEMM_DEBUG_FORCE_PAIR)
+    yield ctx
+    g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
+
+
 def run_guarded(ctx, A, B, bias, epi, stream=None):
     """Run the GEMM into a buffer with 3 guard rows and a 40-element guard tail; check the
     guards and return the M x N result on the host."""
@@ -62,11 +73,13 @@ def check(ctx, M, N, K, epi=g.EPI_NONE, with_bias=False, seed=0, dist="uniform")
 
 # ---- one tile first: pins the UMMA descriptors, TMEM layout and the mbarrier ring ---------
 
-def test_single_tile_single_kblock(ctx):
-    check(ctx, 128, 256, 64)
+def test_single_tile_single_kblock(kctx):
+    check(kctx, 128, 256, 64)
+    check(kctx, 256, 256, 64)
 
 
-def test_single_tile_identity(ctx):
+def test_single_tile_identity(kctx):
+    ctx = kctx
     # A = I (128 x 128) selects B's rows exactly: any descriptor or layout slip shows.
     K = 128
     A = torch.eye(128, K, dtype=torch.float16)
@@ -79,7 +92,8 @@ def test_single_tile_identity(ctx):
     assert torch.equal(C2, A2)
 
 
-def test_all_ones_gives_k(ctx):
+def test_all_ones_gives_k(kctx):
+    ctx = kctx
     for K in (64, 2048):
         A = torch.ones(130, K, dtype=torch.float16)
         B = torch.ones(K, 264, dtype=torch.float16)
@@ -97,26 +111,29 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_ragged_shapes_plain(ctx, shape):
-    check(ctx, *shape, seed=sum(shape))
+def test_ragged_shapes_plain(kctx, shape):
+    check(kctx, *shape, seed=sum(shape))
 
 
 @pytest.mark.parametrize("epi,with_bias", [(g.EPI_NONE, True), (g.EPI_GELU, True), (g.EPI_RELU, True),
                                            (g.EPI_GELU, False), (g.EPI_RELU, False)])
 @pytest.mark.parametrize("shape", [(129, 264, 200), (300, 512, 1024), (8, 2048, 64)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_epilogues(ctx, shape, epi, with_bias):
-    check(ctx, *shape, epi=epi, with_bias=with_bias, seed=shape[0] + 7 * epi)
+def test_epilogues(kctx, shape, epi, with_bias):
+    check(kctx, *shape, epi=epi, with_bias=with_bias, seed=shape[0] + 7 * epi)
 
 
-def test_more_tiles_than_sms(ctx):
-    # 16 x 10 = 160 tiles of 128 x 256 on ~150 SMs, then 32 x 16 = 512 tiles: every CTA
-    # runs several tiles, both TMEM accumulators and many ring phases.
-    check(ctx, 2048, 2560, 256, epi=g.EPI_GELU, with_bias=True, seed=1)
-    check(ctx, 4096, 4096, 128, epi=g.EPI_RELU, with_bias=True, seed=2)
+def test_more_tiles_than_sms(kctx):
+    # 16 x 10 = 160 tiles of 128 x 256 on ~150 SMs (8 x 10 = 80 pair tiles on ~75 pairs),
+    # then 512 (256) tiles: every CTA runs several tiles, both TMEM accumulators and many
+    # ring phases.
+    check(kctx, 2048, 2560, 256, epi=g.EPI_GELU, with_bias=True, seed=1)
+    check(kctx, 4096, 4096, 128, epi=g.EPI_RELU, with_bias=True, seed=2)
+    check(kctx, 4104, 2056, 320, epi=g.EPI_GELU, with_bias=True, seed=4)
 
 
-def test_k_zero_gives_activation_of_bias(ctx):
+def test_k_zero_gives_activation_of_bias(kctx):
+    ctx = kctx
     M, N = 70, 264
     bias = inputs.random_fp16((N,), 9)
     dev = torch.device("cuda:0")
@@ -127,6 +144,35 @@ def test_k_zero_gives_activation_of_bias(ctx):
         ref = oracle_ref(torch.zeros(M, 0, dtype=torch.float16), torch.zeros(0, N, dtype=torch.float16),
                          bias, epi)
         assert_parity(C.cpu().numpy(), ref, f"K=0 epi={epi}")
+
+
+def test_activation_accuracy_on_every_fp16_input(ctx):
+    """K = 0 gives C = act(bias), so the epilogue's activation can be checked value by value:
+    every finite FP16 number in [-12, 12] goes through it. Identity and ReLU must be exact;
+    GELU must be within one FP16 ulp of the FP64 oracle (or 5e-7 absolute, where the result
+    is so small that FP32 rounding of 1 + erf dominates)."""
+    bits = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    vals = bits.view(np.float16)
+    vals = vals[np.isfinite(vals) & (np.abs(vals.astype(np.float64)) <= 12.0)]
+    n = (len(vals) + 7) // 8 * 8
+    bias = np.zeros(n, dtype=np.float16)
+    bias[: len(vals)] = vals
+    dev = torch.device("cuda:0")
+    tb = torch.from_numpy(bias.view(np.int16)).view(torch.float16)
+    for epi in (g.EPI_NONE, g.EPI_RELU, g.EPI_GELU):
+        C = torch.empty(2, n, dtype=torch.float16, device=dev)
+        g.gemm_run(ctx, 2, n, 0, None, None, tb.to(dev), C, epi)
+        torch.cuda.synchronize()
+        got = C.cpu().numpy().astype(np.float64)
+        ref = oracle_ref(torch.zeros(2, 0, dtype=torch.float16), torch.zeros(0, n, dtype=torch.float16),
+                         tb, epi).astype(np.float64)
+        if epi != g.EPI_GELU:
+            assert np.array_equal(got, ref)
+        else:
+            ulp = np.spacing(np.abs(ref).astype(np.float16)).astype(np.float64)
+            err = np.abs(got - ref)
+            bad = err > np.maximum(ulp, 5e-7)
+            assert not bad.any(), (bias[np.nonzero(bad[0])[0][:10]], err[bad][:10])
 
 
 def test_empty_m_or_n_is_a_no_op(ctx):
@@ -192,19 +238,24 @@ def test_bad_arguments_are_rejected_before_launch(ctx):
     torch.cuda.synchronize()
     assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
     assert g.gemm_num_sms(ctx) >= 100
+    assert 0 <= g.gemm_num_pairs(ctx) <= g.gemm_num_sms(ctx) // 2
 
 
-def test_bounded_wait_reports_timeout_and_context_survives(ctx):
+@pytest.mark.parametrize("force", ["single", "pair"])
+def test_bounded_wait_reports_timeout_and_context_survives(ctx, force):
     """The producer withholds its first operand load, so the MMA warp's wait runs out:
     the kernel must return (no hang, no fault) and report GEMM_ERR_TIMEOUT; afterwards the
     same context computes correct results again."""
+    if force == "pair" and g.gemm_num_pairs(ctx) == 0:
+        pytest.skip("the pair kernel cannot run on this device")
+    flag = g.GEMM_DEBUG_FORCE_SINGLE if force == "single" else g.GEMM_DEBUG_FORCE_PAIR
     g.gemm_set_timeout_ns(ctx, 20_000_000)
-    g.gemm_set_debug(ctx, g.GEMM_DEBUG_WITHHOLD_FIRST_LOAD)
+    g.gemm_set_debug(ctx, g.GEMM_DEBUG_WITHHOLD_FIRST_LOAD | flag)
     try:
         dev = torch.device("cuda:0")
-        A = torch.ones(128, 64, dtype=torch.float16, device=dev)
+        A = torch.ones(256, 64, dtype=torch.float16, device=dev)
         B = torch.ones(64, 256, dtype=torch.float16, device=dev)
-        C = torch.zeros(128, 256, dtype=torch.float16, device=dev)
+        C = torch.zeros(256, 256, dtype=torch.float16, device=dev)
         g.gemm(ctx, A, B, None, g.EPI_NONE, out=C)
         torch.cuda.synchronize()
         status, detail = g.gemm_last_device_error(ctx)
