@@ -37,6 +37,7 @@ SIDE_WORKLOADS = ["gemm_8192", "gemm_8192_bias_gelu", "mlp_up_8200x4096x16384_no
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["tensor_core_gemm_tcgen05_gb300/csrc/gemm_kernel.cuh",
+                  "tensor_core_gemm_tcgen05_gb300/csrc/gemm_kernel_pair.cuh",
                   "tensor_core_gemm_tcgen05_gb300/csrc/ptx.cuh",
                   "tensor_core_gemm_tcgen05_gb300/csrc/gemm_api.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_tcgen05_mlp_traffic.txt")
@@ -340,7 +341,7 @@ def run_ours(args):
         "frac": round(per_gpu / peak, 4), "traffic": traffic,
         "peak_source": f"{peak_src} {peak_key} (FP16 = BF16 nominal rate)",
         "traffic_source": traffic_src, "algorithmic_flops_per_launch": w.flops,
-        "algorithmic_bytes_per_launch": w.bytes, "kernel": "gemm_tcgen05_kernel",
+        "algorithmic_bytes_per_launch": w.bytes, "kernel": "gemm_tcgen05_pair_kernel (CTA pairs, 256x256 tiles)",
     }
 
     side = {}
@@ -434,7 +435,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)

@@ -42,6 +42,10 @@ int raster_group(int m_blocks, int64_t a_bytes, int default_group)
     return default_group;
 }
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+// gemm_run_host splits M into at most this many chunks whose uploads, GEMMs and downloads
+// overlap; outputs smaller than kHostChunkMinBytes are not split.
+constexpr int kHostChunksMax = 8;
+constexpr size_t kHostChunkMinBytes = size_t(32) << 20;
 constexpr uint64_t kMinTimeoutNs = 1000000ull;
 
 }  // namespace
@@ -55,9 +59,13 @@ struct gemm_ctx {
     int debug = 0;
     int last_cuda_error = 0;
     int max_clusters = 0;   // co-resident CTA pairs of the pair kernel (0: pair kernel unusable)
-    // staging buffers of gemm_run_host
+    // gemm_run_host: device staging buffers, two copy streams and the events that order
+    // the chunked pipeline (created on first use)
     void *stage = nullptr;
     size_t stage_bytes = 0;
+    cudaStream_t copy_in = nullptr, copy_out = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+    cudaEvent_t ev_in[kHostChunksMax] = {}, ev_mm[kHostChunksMax] = {};
 };
 
 namespace {
@@ -156,6 +164,25 @@ bool encode_2d(gemm_ctx *ctx, CUtensorMap *map, const void *ptr, uint64_t inner,
     return r == CUDA_SUCCESS;
 }
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled while the
+// previous kernel in the stream is finishing and overlaps its own set-up with that tail;
+// it waits (griddepcontrol.wait) before touching global memory.
+void launch_pdl(void (*kernel)(CUtensorMap, CUtensorMap, gb300::GemmParams), int grid, int threads, int smem,
+                cudaStream_t stream, const CUtensorMap &ta, const CUtensorMap &tb, const gb300::GemmParams &p)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, ta, tb, p);
+}
+
 int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, const void *bias, void *C,
            int epilogue, cudaStream_t stream)
 {
@@ -192,14 +219,15 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
         p.num_tiles = p.m_blocks * p.n_blocks;
         p.group_m = raster_group(p.m_blocks, static_cast<int64_t>(M) * K * 2, kPairGroupM);
         const int grid = 2 * std::min(p.num_tiles, ctx->max_clusters);
-        gb300::gemm_tcgen05_pair_kernel<PairCfg><<<grid, PairCfg::NUM_THREADS, PairCfg::SMEM_BYTES, stream>>>(ta, tb, p);
+        launch_pdl(gb300::gemm_tcgen05_pair_kernel<PairCfg>, grid, PairCfg::NUM_THREADS, PairCfg::SMEM_BYTES, stream,
+                   ta, tb, p);
     } else {
         p.m_blocks = (M + Cfg::BM - 1) / Cfg::BM;
         p.n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
         p.num_tiles = p.m_blocks * p.n_blocks;
         p.group_m = raster_group(p.m_blocks, static_cast<int64_t>(M) * K * 2, kGroupM);
         const int grid = std::min(p.num_tiles, ctx->num_sms);
-        gb300::gemm_tcgen05_kernel<Cfg><<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, p);
+        launch_pdl(gb300::gemm_tcgen05_kernel<Cfg>, grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream, ta, tb, p);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -303,6 +331,22 @@ int gemm_run_host(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A,
     DeviceGuard guard(ctx->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    if (!ctx->copy_in) {   // first call: the pipeline's streams and events
+        e = cudaStreamCreateWithFlags(&ctx->copy_in, cudaStreamNonBlocking);
+        if (e == cudaSuccess)
+            e = cudaStreamCreateWithFlags(&ctx->copy_out, cudaStreamNonBlocking);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&ctx->ev_start, cudaEventDisableTiming);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&ctx->ev_done, cudaEventDisableTiming);
+        for (int i = 0; i < kHostChunksMax && e == cudaSuccess; ++i) {
+            e = cudaEventCreateWithFlags(&ctx->ev_in[i], cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&ctx->ev_mm[i], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess)
+            return cuda_fail(ctx, e, GEMM_ERR_NOMEM);
+    }
     if (need > ctx->stage_bytes) {
         if (ctx->stage) {
             cudaStreamSynchronize(s);
@@ -318,22 +362,49 @@ int gemm_run_host(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A,
         ctx->stage_bytes = need;
     }
     char *base = static_cast<char *>(ctx->stage);
-    void *dA = base, *dB = base + round256(a_b);
-    void *dbias = bias ? base + round256(a_b) + round256(b_b) : nullptr;
-    void *dC = base + round256(a_b) + round256(b_b) + round256(bias_b);
-    if (a_b && (e = cudaMemcpyAsync(dA, A, a_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    char *dA = base, *dB = base + round256(a_b);
+    char *dbias = bias ? base + round256(a_b) + round256(b_b) : nullptr;
+    char *dC = base + round256(a_b) + round256(b_b) + round256(bias_b);
+
+    // Chunks of whole 256-row tiles: the upload of chunk i+1, the GEMM of chunk i and the
+    // download of chunk i-1 run at the same time (copy_in, s, copy_out). B and the bias go
+    // first, on s, since every chunk needs them.
+    int chunks = c_b < kHostChunkMinBytes ? 1 : 4;
+    int64_t rows = (M + chunks - 1) / chunks;
+    rows = (rows + 255) / 256 * 256;
+    chunks = static_cast<int>((M + rows - 1) / rows);
+    if ((e = cudaEventRecord(ctx->ev_start, s)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ctx->copy_in, ctx->ev_start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ctx->copy_out, ctx->ev_start, 0)) != cudaSuccess)
         return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
     if (b_b && (e = cudaMemcpyAsync(dB, B, b_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
         return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
     if (bias_b && (e = cudaMemcpyAsync(dbias, bias, bias_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
         return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
-    rc = launch(ctx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), K ? dA : nullptr,
-                K ? dB : nullptr, dbias, dC, epilogue, s);
-    if (rc != GEMM_OK)
-        return rc;
-    if ((e = cudaMemcpyAsync(C, dC, c_b, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-        return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
-    if ((e = cudaStreamSynchronize(s)) != cudaSuccess)
+    for (int i = 0; i < chunks; ++i) {
+        const int64_t r0 = i * rows, mi = std::min<int64_t>(rows, M - r0);
+        const size_t a_off = static_cast<size_t>(r0) * K * 2, c_off = static_cast<size_t>(r0) * N * 2;
+        const size_t a_len = static_cast<size_t>(mi) * K * 2, c_len = static_cast<size_t>(mi) * N * 2;
+        if (a_len && (e = cudaMemcpyAsync(dA + a_off, static_cast<const char *>(A) + a_off, a_len,
+                                          cudaMemcpyHostToDevice, ctx->copy_in)) != cudaSuccess)
+            return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+        if ((e = cudaEventRecord(ctx->ev_in[i], ctx->copy_in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(s, ctx->ev_in[i], 0)) != cudaSuccess)
+            return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+        rc = launch(ctx, static_cast<int>(mi), static_cast<int>(N), static_cast<int>(K), K ? dA + a_off : nullptr,
+                    K ? dB : nullptr, dbias, dC + c_off, epilogue, s);
+        if (rc != GEMM_OK)
+            return rc;
+        if ((e = cudaEventRecord(ctx->ev_mm[i], s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(ctx->copy_out, ctx->ev_mm[i], 0)) != cudaSuccess)
+            return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+        if ((e = cudaMemcpyAsync(static_cast<char *>(C) + c_off, dC + c_off, c_len, cudaMemcpyDeviceToHost,
+                                 ctx->copy_out)) != cudaSuccess)
+            return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+    }
+    if ((e = cudaEventRecord(ctx->ev_done, ctx->copy_out)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, ctx->ev_done, 0)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess)
         return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
     return gemm_last_device_error(ctx, nullptr);
 }
@@ -366,6 +437,20 @@ int gemm_destroy(gemm_ctx *ctx)
             cudaFree(ctx->d_err);
         if (ctx->stage)
             cudaFree(ctx->stage);
+        for (int i = 0; i < kHostChunksMax; ++i) {
+            if (ctx->ev_in[i])
+                cudaEventDestroy(ctx->ev_in[i]);
+            if (ctx->ev_mm[i])
+                cudaEventDestroy(ctx->ev_mm[i]);
+        }
+        if (ctx->ev_start)
+            cudaEventDestroy(ctx->ev_start);
+        if (ctx->ev_done)
+            cudaEventDestroy(ctx->ev_done);
+        if (ctx->copy_in)
+            cudaStreamDestroy(ctx->copy_in);
+        if (ctx->copy_out)
+            cudaStreamDestroy(ctx->copy_out);
         cudaGetLastError();
     }
     delete ctx;

@@ -80,8 +80,10 @@ struct KernelConfig {
     static constexpr int EPI_COL_GROUPS = NUM_EPI_WARPS / 4;   // warps sharing a TMEM quarter
     static constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
-    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES +
-                                      NUM_BARS * 8 + 64;
+    // after the ring: barriers, TMEM address, stop flag; then one BN-wide bias slice per
+    // epilogue warp (FP16)
+    static constexpr int BIAS_OFFSET = STAGES * STAGE_BYTES + ((NUM_BARS * 8 + 16 + 15) / 16) * 16;
+    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + BIAS_OFFSET + NUM_EPI_WARPS * BN * 2;
 
     static_assert(BM == 128, "one CTA, M = 128: TMEM lane i holds tile row i");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
@@ -195,38 +197,53 @@ __device__ __forceinline__ float gelu_erf(float x)
 }
 #endif
 
-// One 32-column chunk of one accumulator row per thread: TMEM -> registers (tcgen05.ld),
-// + bias, activation, FP32 -> FP16 (round to nearest even), four 16-byte stores.
-// Called by all 32 lanes of an epilogue warp together (tcgen05.ld is warp-collective);
-// `row_ok` masks rows >= M, and column groups of 8 at or past N are skipped.
-__device__ __forceinline__ void epilogue_chunk(const GemmParams &p, uint32_t taddr, int n0, __half *crow,
-                                               bool row_ok)
+// Same as tcgen05.wait::ld, and ties the 32 destination registers of the load it waits
+// for to this point, so that no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32])
 {
-    uint32_t r[32];
-    if (p.num_kb > 0) {
-        tmem_ld_32x32b_x32(taddr, r);
-        tmem_ld_wait();
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            r[j] = 0u;   // K = 0: the empty sum
-    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                   "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+                   "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// Epilogue of one warp for one tile, step 1 (before the accumulator is ready): lane l
+// fetches the bias of tile columns [8l, 8l+8) (columns at or past N read as 0) into
+// registers; the load's latency hides behind the wait for the accumulator.
+__device__ __forceinline__ uint4 bias_fetch(const GemmParams &p, int n_tile0, int lane)
+{
+    uint4 bv = make_uint4(0u, 0u, 0u, 0u);
+    const int n = n_tile0 + 8 * lane;
+    if (p.bias != nullptr && n < p.N)
+        bv = __ldg(reinterpret_cast<const uint4 *>(p.bias + n));
+    return bv;
+}
+
+// One 32-column chunk of one accumulator row per thread: + bias (from this warp's staged
+// slice in shared memory), activation in FP32, FP32 -> FP16 (round to nearest even), four
+// 16-byte streaming stores (C is written once and never re-read). `row_ok` masks rows >= M;
+// column groups of 8 at or past N are skipped.
+__device__ __forceinline__ void epilogue_math_store(const GemmParams &p, const uint32_t (&r)[32], const uint4 *sbias,
+                                                    int n0, __half *crow, bool row_ok)
+{
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
         v[j] = __uint_as_float(r[j]);
-    if (p.bias != nullptr) {
+    if (sbias != nullptr) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            if (n0 + 8 * i < p.N) {
-                const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(p.bias + n0 + 8 * i));
-                const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
+            const uint4 bv = sbias[i];
+            const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(bh[e]);
-                    v[8 * i + 2 * e] += f.x;
-                    v[8 * i + 2 * e + 1] += f.y;
-                }
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(bh[e]);
+                v[8 * i + 2 * e] += f.x;
+                v[8 * i + 2 * e + 1] += f.y;
             }
         }
     }
@@ -252,8 +269,47 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams &p, uint32_t tad
                 out.y = *reinterpret_cast<uint32_t *>(&h1);
                 out.z = *reinterpret_cast<uint32_t *>(&h2);
                 out.w = *reinterpret_cast<uint32_t *>(&h3);
-                *reinterpret_cast<uint4 *>(crow + n0 + 8 * i) = out;
+                __stcs(reinterpret_cast<uint4 *>(crow + n0 + 8 * i), out);
             }
+        }
+    }
+}
+
+// Epilogue of one warp for one tile, step 2 (accumulator ready): up to CHUNKS chunks of 32
+// columns starting at TMEM address `taddr` / output column `n_first`. The TMEM load of chunk
+// c+1 is in flight while chunk c is processed. Called by all 32 lanes together
+// (tcgen05.ld is warp-collective; the chunk count is the same for every lane).
+template <int CHUNKS>
+__device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t taddr, int n_first, __half *crow,
+                                              bool row_ok, const uint4 *sbias)
+{
+    const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
+    if (valid <= 0)
+        return;
+    const bool has_acc = p.num_kb > 0;   // K = 0: the empty sum, no accumulator to read
+    uint32_t ra[32], rb[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        ra[j] = 0u;
+        rb[j] = 0u;
+    }
+    if (has_acc)
+        tmem_ld_32x32b_x32(taddr, ra);
+#pragma unroll 1
+    for (int c = 0; c < valid; c += 2) {
+        if (has_acc) {
+            tmem_ld_wait_regs(ra);
+            if (c + 1 < valid)
+                tmem_ld_32x32b_x32(taddr + 32u * (c + 1), rb);
+        }
+        epilogue_math_store(p, ra, sbias ? sbias + 4 * c : nullptr, n_first + 32 * c, crow, row_ok);
+        if (c + 1 < valid) {
+            if (has_acc) {
+                tmem_ld_wait_regs(rb);
+                if (c + 2 < valid)
+                    tmem_ld_32x32b_x32(taddr + 32u * (c + 2), ra);
+            }
+            epilogue_math_store(p, rb, sbias ? sbias + 4 * (c + 1) : nullptr, n_first + 32 * (c + 1), crow, row_ok);
         }
     }
 }
@@ -280,6 +336,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const uint32_t drain = acce0 + 8u * Cfg::ACC_BUFS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    uint4 *bias_stage = reinterpret_cast<uint4 *>(sp + Cfg::BIAS_OFFSET);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -309,6 +366,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above (barrier set-up, Tensor Memory allocation, descriptor prefetch) may
+    // overlap the previous kernel in the stream; no global memory is touched before this.
+    grid_dependency_wait();
+    grid_dependents_launch();
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
 
     if (warp == 0) {
@@ -408,11 +469,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         constexpr int CHUNKS = BN / 32 / Cfg::EPI_COL_GROUPS;   // 32-column chunks per warp
         const int c_begin = ((warp - 2) >> 2) * CHUNKS;
+        uint4 *my_bias = bias_stage + (warp - 2) * (BN / 8);   // this warp's BN-wide bias slice
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
             int mb, nb;
             tile_coords(p, t, mb, nb);
+            const uint4 bv = bias_fetch(p, nb * BN, lane);
             int ok = 1;
             if (lane == 0)
                 ok = wait_bounded(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
@@ -420,16 +483,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             if (!ok)
                 break;
             tc_fence_after_sync();
-            const int row = mb * BM + quarter * 32 + lane;
-            const bool row_ok = row < p.M;
-            __half *crow = p.C + static_cast<int64_t>(row) * p.N;
-#pragma unroll 1
-            for (int c = c_begin; c < c_begin + CHUNKS; ++c) {
-                const int n0 = nb * BN + c * 32;
-                if (n0 >= p.N)
-                    break;
-                epilogue_chunk(p, tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c * 32), n0, crow, row_ok);
+            if (p.bias != nullptr) {
+                my_bias[lane] = bv;
+                __syncwarp();
             }
+            const int row = mb * BM + quarter * 32 + lane;
+            __half *crow = p.C + static_cast<int64_t>(row) * p.N;
+            epilogue_tile<CHUNKS>(p, tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c_begin * 32),
+                                  nb * BN + c_begin * 32, crow, row < p.M,
+                                  p.bias != nullptr ? my_bias + c_begin * 4 : nullptr);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)

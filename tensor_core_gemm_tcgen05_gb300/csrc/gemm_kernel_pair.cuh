@@ -14,7 +14,7 @@
 //    the "empty" and "accumulator full" barriers of both CTAs (multicast); both CTAs'
 //    epilogue warps arrive on CTA 0's "accumulator empty" barrier.
 //  * Each CTA's epilogue warps drain their own Tensor Memory exactly as in the one-CTA
-//    kernel (epilogue_chunk), overlapping the next tile's MMAs (two accumulators).
+//    kernel (epilogue_tile), overlapping the next tile's MMAs (two accumulators).
 // Waits are bounded as in the one-CTA kernel; a CTA that gives up also raises the stop
 // flag of its peer, and both CTAs meet at a cluster barrier before Tensor Memory is freed.
 #pragma once
@@ -44,7 +44,8 @@ struct PairConfig {
     static constexpr int EPI_COL_GROUPS = NUM_EPI_WARPS / 4;
     static constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
+    static constexpr int BIAS_OFFSET = STAGES * STAGE_BYTES + ((NUM_BARS * 8 + 16 + 15) / 16) * 16;
+    static constexpr int SMEM_BYTES = 1024 + BIAS_OFFSET + NUM_EPI_WARPS * BN * 2;
 
     static_assert(BN % 128 == 0 && BN >= 128 && BN <= 256, "UMMA N for M = 256, two 64-column boxes per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM alloc size");
@@ -106,6 +107,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
     const uint32_t drain = acce0 + 8u * Cfg::ACC_BUFS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    uint4 *bias_stage = reinterpret_cast<uint4 *>(sp + Cfg::BIAS_OFFSET);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -141,6 +143,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above (barrier set-up, Tensor Memory allocation, descriptor prefetch) may
+    // overlap the previous kernel in the stream; no global memory is touched before this.
+    grid_dependency_wait();
+    grid_dependents_launch();
     const uint32_t full0_leader = mapa_shared(full0, 0);
     const uint32_t acce0_leader = mapa_shared(acce0, 0);
     const PairWaitCtl wc{abort_flag, mapa_shared(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u), p.err,
@@ -248,11 +254,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         constexpr int CHUNKS = BN / 32 / Cfg::EPI_COL_GROUPS;
         const int c_begin = ((warp - 2) >> 2) * CHUNKS;
+        uint4 *my_bias = bias_stage + (warp - 2) * (BN / 8);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
             int mb, nb;
             tile_coords(p, t, mb, nb);
+            const uint4 bv = bias_fetch(p, nb * BN, lane);
             int ok = 1;
             if (lane == 0)
                 ok = pair_wait(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
@@ -260,17 +268,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
             if (!ok)
                 break;
             tc_fence_after_sync();
-            const int row = mb * BM + static_cast<int>(rank) * Cfg::CTA_BM + quarter * 32 + lane;
-            const bool row_ok = row < p.M;
-            __half *crow = p.C + static_cast<int64_t>(row) * p.N;
-#pragma unroll 1
-            for (int c = c_begin; c < c_begin + CHUNKS; ++c) {
-                const int n0 = nb * BN + c * 32;
-                if (n0 >= p.N)
-                    break;
-                epilogue_chunk(p, tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c * 32), n0, crow,
-                               row_ok);
+            if (p.bias != nullptr) {
+                my_bias[lane] = bv;
+                __syncwarp();
             }
+            const int row = mb * BM + static_cast<int>(rank) * Cfg::CTA_BM + quarter * 32 + lane;
+            __half *crow = p.C + static_cast<int64_t>(row) * p.N;
+            epilogue_tile<CHUNKS>(p, tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c_begin * 32),
+                                  nb * BN + c_begin * 32, crow, row < p.M,
+                                  p.bias != nullptr ? my_bias + c_begin * 4 : nullptr);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)

@@ -100,6 +100,22 @@ __device__ __forceinline__ void cluster_sync()
                      : "memory");
 }
 
+// ---- programmatic dependent launch --------------------------------------------------------
+// Block until the grids this one depends on (the previous kernel in the stream, when it was
+// launched with programmatic stream serialisation) have completed and their memory is
+// visible. A no-op for a normal launch.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream (if launched as a programmatic dependent) to start
+// its own set-up now; it still waits in grid_dependency_wait for this grid to finish.
+__device__ __forceinline__ void grid_dependents_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- TMA -------------------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const void *map)
 {

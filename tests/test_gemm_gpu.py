@@ -280,6 +280,17 @@ def test_host_buffer_entry_point(ctx):
     C2 = torch.empty(M, N, dtype=torch.float16)
     g.gemm_run_host(ctx, M, N, K, A.clone(), B.clone(), None, C2, g.EPI_RELU)
     assert_parity(C2.numpy(), oracle_ref(A, B, None, g.EPI_RELU), "gemm_run_host pageable")
+    # an output above 32 MiB is pipelined in 4 row chunks (the last one ragged)
+    M, N, K = 4100, 4096, 512
+    A = inputs.random_fp16((M, K), 74).pin_memory()
+    B = inputs.random_fp16((K, N), 75).pin_memory()
+    bias = inputs.random_fp16((N,), 76).pin_memory()
+    C = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+    g.gemm_run_host(ctx, M, N, K, A, B, bias, C, g.EPI_GELU)
+    rows = inputs.sample_rows(M, 300, seed=8, include_last=8).numpy()
+    rows = np.union1d(rows, [0, 1279, 1280, 2559, 2560, 3839, 3840])
+    assert bool(torch.isfinite(C).all())
+    assert_parity(C.numpy()[rows], oracle_ref(A, B, bias, g.EPI_GELU, rows=rows), "gemm_run_host chunked")
 
 
 def test_side_stream_and_cuda_graph(ctx):
