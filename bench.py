@@ -233,6 +233,72 @@ def device_buffers(w, device):
     return (A, B, bias), (dA, dB, dbias, dC)
 
 
+SOFTMAX_SHAPE = (8192, 16384)   # the MLP output's shape: 268 MB in, 268 MB out
+
+
+def measure_softmax(g, ctx, stream, device, peaks, steps=50):
+    """Row-wise softmax (the next hot-path row): HBM-bound, so GB/s against the measured copy
+    bandwidth; algorithmic bytes = one read and one write of every FP16 element."""
+    import torch
+    from tensor_core_gemm_tcgen05_gb300 import inputs
+    rows, cols = SOFTMAX_SHAPE
+    X = (inputs.random_fp16((rows, cols), 4242) * 8).to(device)
+    Y = torch.empty_like(X)
+    for _ in range(5):
+        g.gemm_row_softmax(ctx, rows, cols, X, Y, stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.gemm_row_softmax(ctx, rows, cols, X, Y, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / steps * 1e3
+    nbytes = 2 * rows * cols * 2
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {f"row_softmax_{rows}x{cols}": {
+        "us_per_launch": round(us, 2), "GB/s": round(gbs, 1), "bound": "hbm",
+        "frac_of_measured_hbm": round(gbs / float(peaks["hbm_gbs"]), 4),
+        "algorithmic_bytes_per_launch": nbytes}}
+
+
+def measure_fused_softmax(g, ctx, stream, device, peaks, steps=30):
+    """GEMM with the row-softmax epilogue on attention-score shapes (HBM-bound: the logits
+    never leave the SM), against the same result computed unfused (GEMM, then the row
+    softmax in place: C is written, read and written again)."""
+    import torch
+    from tensor_core_gemm_tcgen05_gb300 import inputs
+    w = inputs.WORKLOADS["scores_262144x256x128_softmax"]
+    _, (dA, dB, dbias, dC) = device_buffers(w, device)
+
+    def fused():
+        g.gemm_run(ctx, w.M, w.N, w.K, dA, dB, dbias, dC, g.EPI_SOFTMAX, stream)
+
+    def unfused():
+        g.gemm_run(ctx, w.M, w.N, w.K, dA, dB, dbias, dC, g.EPI_NONE, stream)
+        g.gemm_row_softmax(ctx, w.M, w.N, dC, dC, stream)
+
+    out = {}
+    for name, fn in (("fused", fused), ("unfused", unfused)):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) / steps * 1e3
+    gbs = w.bytes / (out["fused"] * 1e-6) / 1e9
+    return {w.name: {
+        "us_per_launch": round(out["fused"], 2), "unfused_us": round(out["unfused"], 2),
+        "GB/s": round(gbs, 1), "bound": "hbm", "frac_of_measured_hbm": round(gbs / float(peaks["hbm_gbs"]), 4),
+        "tflops": round(w.flops / (out["fused"] * 1e-6) / 1e12, 1), "algorithmic_bytes_per_launch": w.bytes}}
+
+
 def measure_e2e(g, ctx, w, host, stream, steps):
     """Same metric through gemm_run_host: pinned host inputs copied in, C copied out, every
     step inside the timed region (host wall clock around synchronous calls)."""
@@ -358,6 +424,8 @@ def run_ours(args):
                           "pct_of_burst_peak": round(100 * tf / float(peaks["bf16_tflops"]), 2)}
             del a, b, bi, c
         torch.cuda.empty_cache()
+        side.update(measure_softmax(g, ctx, stream, device, peaks))
+        side.update(measure_fused_softmax(g, ctx, stream, device, peaks))
 
     e2e = None if args.no_e2e else measure_e2e(g, ctx, w, host, stream, steps=max(3, min(args.steps, 10)))
     base = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, host)

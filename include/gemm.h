@@ -39,7 +39,13 @@ typedef struct gemm_ctx gemm_ctx;
 enum gemm_epilogue {
     GEMM_EPI_NONE = 0, /* C = A*B (+ bias)                                           */
     GEMM_EPI_GELU = 1, /* C = GELU_erf(A*B (+ bias))                                 */
-    GEMM_EPI_RELU = 2  /* C = max(A*B (+ bias), 0)                                   */
+    GEMM_EPI_RELU = 2, /* C = max(A*B (+ bias), 0)                                   */
+    GEMM_EPI_SOFTMAX = 3 /* C[r][:] = softmax over the row of A*B (+ bias): the logits stay
+                            in FP32 inside the kernel and are never written. Needs
+                            N <= 256 (one tile spans the whole row); larger N returns
+                            GEMM_ERR_ARG (run GEMM_EPI_NONE, then gemm_row_softmax).
+                            "Designing High-Performance GPU Kernels with TileLang"
+                            (spaxe.top): row-wise softmax in the GEMM epilogue.       */
 };
 
 /* Status codes. Every error is detected before anything is enqueued: on error nothing
@@ -124,6 +130,18 @@ int gemm_num_sms(gemm_ctx *ctx);
  * one-CTA kernel). gemm_run picks the pair kernel when the problem has at least this many
  * 256 x 256 tiles, else the one-CTA kernel (128 x 256 tiles). */
 int gemm_num_pairs(gemm_ctx *ctx);
+
+/* Row-wise softmax: Y[r][j] = exp(X[r][j] - m_r) / sum_k exp(X[r][k] - m_r), m_r the row
+ * maximum ("TileLang: Criando Kernels de GPU ..." (noticiai.com.br), section "Softmax por
+ * linha e FlashAttention": per row the maximum, subtraction, exponential and
+ * normalisation; "TileLang ..." (pro.edgex.exchange): max and sum reductions in registers).
+ *   rows, cols: 0 <= rows, 0 <= cols <= 2^31 - 1; either 0 is a no-op. cols must be a
+ *               multiple of 8.
+ *   X, Y      : device pointers (the context's device), rows x cols FP16 row-major,
+ *               16-byte aligned. Y may be X itself (in place) but may not partly overlap it.
+ * FP32 arithmetic, one RNE rounding to FP16. Entries of -inf contribute 0 (a row that is
+ * all -inf gives NaN). Asynchronous on `stream`; allocates nothing; one kernel launch. */
+int gemm_row_softmax(gemm_ctx *ctx, int64_t rows, int64_t cols, const void *X, void *Y, void *stream);
 
 /* Test hooks (no effect on results when left at their defaults).
  *   gemm_set_timeout_ns: the limit of every in-kernel wait (default 2e9 ns; values below

@@ -24,7 +24,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-ACT_NONE, ACT_GELU, ACT_RELU = 0, 1, 2
+ACT_NONE, ACT_GELU, ACT_RELU, ACT_SOFTMAX = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -50,6 +50,9 @@ def _load():
             lib.oracle_act.restype = ctypes.c_double
             lib.oracle_act.argtypes = [ctypes.c_double, ctypes.c_int]
             lib.oracle_default_threads.restype = ctypes.c_int
+            lib.oracle_softmax_rows.restype = ctypes.c_int
+            lib.oracle_softmax_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.oracle_gemm_rows.restype = ctypes.c_int
             lib.oracle_gemm_rows.argtypes = [
                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
@@ -121,3 +124,18 @@ def gemm(A, B, bias=None, act_code: int = ACT_NONE, rows=None, threads: int = 0,
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_rows failed with code {rc}")
     return out_h.view(np.float16), out_d, used.value
+
+
+def softmax_rows(X, threads: int = 0, want_f64: bool = False):
+    """Oracle row-wise softmax of a 2-D FP16 array: returns ``(Y fp16, Y_f64 or None)``."""
+    x = _u16(X)
+    if x.ndim != 2:
+        raise ValueError("X must be 2-D")
+    rows, cols = x.shape
+    y = np.empty((rows, cols), dtype=np.uint16)
+    yd = np.empty((rows, cols), dtype=np.float64) if want_f64 else None
+    rc = _load().oracle_softmax_rows(rows, cols, x.ctypes.data, y.ctypes.data,
+                                     None if yd is None else yd.ctypes.data, int(threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_softmax_rows failed with code {rc}")
+    return y.view(np.float16), yd

@@ -25,6 +25,10 @@
  *      form; the pages only say "GELU"), or ReLU(x) = max(x, 0).
  *  - The result is rounded once to FP16, round-to-nearest-even, with overflow to +-inf.
  *
+ * The file also holds the row-wise softmax of the same tutorial (oracle_softmax_rows), and
+ * the GEMM with a row-softmax epilogue (act = 3): softmax over each row of A*B + bias, the
+ * logits kept in double (never rounded to FP16).
+ *
  * Parity pins (tests/test_oracle.py): exhaustive FP16 decoding and RNE encoding against
  * numpy; a textbook worked example; identity and all-ones products; brute-force loops on
  * tiny shapes; numpy float64 matmul on medium shapes; GELU against standard-normal table
@@ -40,7 +44,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORACLE_ACT_NONE = 0, ORACLE_ACT_GELU = 1, ORACLE_ACT_RELU = 2 };
+enum { ORACLE_ACT_NONE = 0, ORACLE_ACT_GELU = 1, ORACLE_ACT_RELU = 2, ORACLE_ACT_SOFTMAX = 3 };
 
 /* ---- FP16 (IEEE 754 binary16) <-> double, written from the format's definition ---------
  * binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
@@ -113,6 +117,74 @@ int oracle_default_threads(void)
     return n > 0 ? (int)n : 1;
 }
 
+/* ---- row-wise softmax ---------------------------------------------------------------------
+ * Y[r][j] = fp16_rne( exp(x[r][j] - m_r) / sum_k exp(x[r][k] - m_r) ),  m_r = max_k x[r][k],
+ * with x the FP16 input widened exactly to double and everything in double ("TileLang:
+ * Criando Kernels de GPU ..." (noticiai.com.br), section "Softmax por linha e
+ * FlashAttention": per row, the maximum, subtraction, exponentiation, normalisation).
+ * Subtracting the row maximum does not change the mathematical result; it keeps exp() in
+ * range. A row of length 0 has nothing to write. */
+typedef struct {
+    int64_t rows, cols;
+    const uint16_t *X;
+    uint16_t *Y;
+    double *Yd;   /* rows x cols doubles before rounding, or NULL */
+    int tid, nthreads;
+} softmax_job_t;
+
+static void *softmax_worker(void *arg)
+{
+    softmax_job_t *j = (softmax_job_t *)arg;
+    for (int64_t r = j->tid; r < j->rows; r += j->nthreads) {
+        const uint16_t *x = j->X + r * j->cols;
+        double m = -INFINITY;
+        for (int64_t c = 0; c < j->cols; ++c) {
+            const double v = oracle_half_to_double(x[c]);
+            if (v > m)
+                m = v;
+        }
+        double s = 0.0;
+        for (int64_t c = 0; c < j->cols; ++c)
+            s += exp(oracle_half_to_double(x[c]) - m);
+        for (int64_t c = 0; c < j->cols; ++c) {
+            const double y = exp(oracle_half_to_double(x[c]) - m) / s;
+            if (j->Yd)
+                j->Yd[r * j->cols + c] = y;
+            j->Y[r * j->cols + c] = oracle_double_to_half(y);
+        }
+    }
+    return NULL;
+}
+
+/* Softmax of each of the `rows` rows of X (rows x cols FP16 bits, row-major) into Y (same
+ * shape); Yd (optional) receives the values before rounding. Returns 0 or -1 (bad args). */
+int oracle_softmax_rows(int64_t rows, int64_t cols, const uint16_t *X, uint16_t *Y, double *Yd, int threads)
+{
+    if (rows < 0 || cols < 0 || ((rows * cols > 0) && (!X || !Y)))
+        return -1;
+    if (rows == 0 || cols == 0)
+        return 0;
+    int T = threads > 0 ? threads : oracle_default_threads();
+    if (T > rows)
+        T = (int)rows;
+    pthread_t *th = (pthread_t *)malloc((size_t)T * sizeof(pthread_t));
+    softmax_job_t *jobs = (softmax_job_t *)calloc((size_t)T, sizeof(softmax_job_t));
+    if (!th || !jobs) {
+        free(th);
+        free(jobs);
+        return -2;
+    }
+    for (int t = 0; t < T; ++t) {
+        jobs[t] = (softmax_job_t){rows, cols, X, Y, Yd, t, T};
+        pthread_create(&th[t], NULL, softmax_worker, &jobs[t]);
+    }
+    for (int t = 0; t < T; ++t)
+        pthread_join(th[t], NULL);
+    free(th);
+    free(jobs);
+    return 0;
+}
+
 /* ---- the GEMM --------------------------------------------------------------------------- */
 typedef struct {
     int64_t N, K;
@@ -149,6 +221,26 @@ static void *row_worker(void *arg)
             for (int64_t n = 0; n < N; ++n)
                 acc[n] += a * brow[n];
         }
+        if (j->act == ORACLE_ACT_SOFTMAX) {
+            /* softmax over the whole output row of logits acc[n] + beta[n], in double
+             * ("Designing High-Performance GPU Kernels with TileLang", spaxe.top: row-wise
+             * softmax applied to the GEMM result in its epilogue) */
+            double mx = -INFINITY, sum = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                acc[n] += (j->biasd ? j->biasd[n] : 0.0);
+                if (acc[n] > mx)
+                    mx = acc[n];
+            }
+            for (int64_t n = 0; n < N; ++n)
+                sum += exp(acc[n] - mx);
+            for (int64_t n = 0; n < N; ++n) {
+                const double y = exp(acc[n] - mx) / sum;
+                if (j->out_d)
+                    j->out_d[i * N + n] = y;
+                j->out_h[i * N + n] = oracle_double_to_half(y);
+            }
+            continue;
+        }
         for (int64_t n = 0; n < N; ++n) {
             double x = acc[n] + (j->biasd ? j->biasd[n] : 0.0);
             x = oracle_act(x, j->act);
@@ -183,7 +275,8 @@ static void *widen_worker(void *arg)
  * Compute the rows `rows[0..nrows)` of C = act(A*B + bias) (all M rows, in order, when
  * rows == NULL; then nrows must equal M).
  *   A    : M x K FP16 bits, row-major        B : K x N FP16 bits, row-major
- *   bias : N FP16 bits, or NULL (no bias)    act : 0 none, 1 GELU (erf), 2 ReLU
+ *   bias : N FP16 bits, or NULL (no bias)    act : 0 none, 1 GELU (erf), 2 ReLU,
+ *                                             3 softmax over each output row
  *   out_h: nrows x N FP16 bits (row i of out_h is row rows[i] of C)
  *   out_d: nrows x N doubles before rounding, or NULL
  *   threads: worker threads (<= 0: all online cores); *threads_used receives the count.
@@ -193,7 +286,7 @@ int oracle_gemm_rows(int64_t M, int64_t N, int64_t K, const uint16_t *A, const u
                      const uint16_t *bias, int act, const int64_t *rows, int64_t nrows,
                      uint16_t *out_h, double *out_d, int threads, int *threads_used)
 {
-    if (M < 0 || N < 0 || K < 0 || nrows < 0 || act < 0 || act > 2 || !out_h)
+    if (M < 0 || N < 0 || K < 0 || nrows < 0 || act < 0 || act > 3 || !out_h)
         return -1;
     if ((M * K > 0 && !A) || (K * N > 0 && !B))
         return -1;

@@ -19,12 +19,12 @@ import ctypes
 import os
 import threading
 
-from .inputs import EPI_GELU, EPI_NONE, EPI_RELU  # noqa: F401  (C ABI epilogue codes)
+from .inputs import EPI_GELU, EPI_NONE, EPI_RELU, EPI_SOFTMAX  # noqa: F401  (C ABI epilogue codes)
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgb300gemm.so")
 
-GEMM_EPI_NONE, GEMM_EPI_GELU, GEMM_EPI_RELU = EPI_NONE, EPI_GELU, EPI_RELU
+GEMM_EPI_NONE, GEMM_EPI_GELU, GEMM_EPI_RELU, GEMM_EPI_SOFTMAX = EPI_NONE, EPI_GELU, EPI_RELU, EPI_SOFTMAX
 GEMM_OK = 0
 GEMM_ERR_ARG = -1
 GEMM_ERR_ALIGN = -2
@@ -42,6 +42,7 @@ EXPORTS = (
     "gemm_create", "gemm_run", "gemm_run_host", "gemm_last_device_error",
     "gemm_last_cuda_error", "gemm_destroy", "gemm_status_string", "gemm_num_sms",
     "gemm_set_timeout_ns", "gemm_set_debug", "gemm_run_noalloc", "gemm_num_pairs",
+    "gemm_row_softmax",
 )
 GEMM_NOALLOC_SCRATCH_BYTES = 256
 
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
             L.gemm_status_string.restype = ctypes.c_char_p
             L.gemm_num_sms.argtypes = [vp]
             L.gemm_num_pairs.argtypes = [vp]
+            L.gemm_row_softmax.argtypes = [vp, i64, i64, vp, vp, vp]
             L.gemm_set_timeout_ns.argtypes = [vp, ctypes.c_uint64]
             L.gemm_set_debug.argtypes = [vp, i32]
             L.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, i32, vp]
@@ -200,6 +202,27 @@ def gemm_num_sms(ctx) -> int:
 
 def gemm_num_pairs(ctx) -> int:
     return int(lib().gemm_num_pairs(_h(ctx)))
+
+
+def gemm_row_softmax(ctx, rows, cols, X, Y, stream=None) -> int:
+    rc = lib().gemm_row_softmax(_h(ctx), rows, cols, _ptr(X), _ptr(Y), _stream(stream, _dev(ctx)))
+    return _check(rc, "gemm_row_softmax")
+
+
+def row_softmax(ctx, X, out=None, stream=None):
+    """Row-wise softmax of a 2-D torch CUDA FP16 tensor through ``gemm_row_softmax``."""
+    import torch
+
+    rows, cols = X.shape
+    if out is None:
+        out = torch.empty_like(X)
+    for t in (X, out):
+        if t.dtype != torch.float16 or not t.is_contiguous():
+            raise ValueError("X and out must be contiguous float16 tensors")
+    if stream is None:
+        stream = torch.cuda.current_stream(X.device)
+    gemm_row_softmax(ctx, rows, cols, X, out, stream)
+    return out
 
 
 def gemm_set_timeout_ns(ctx, ns: int) -> int:

@@ -12,6 +12,7 @@
 #include "gemm.h"
 #include "gemm_kernel.cuh"
 #include "gemm_kernel_pair.cuh"
+#include "softmax_kernel.cuh"
 
 namespace {
 
@@ -23,25 +24,23 @@ using Cfg = gb300::KernelConfig<128, 256, 4, GB300_EPI_WARPS>;
 #define GB300_PAIR_STAGES 6
 #endif
 using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS>;
-constexpr int kGroupM = 16;
-#ifndef GB300_PAIR_GROUP_M
-#define GB300_PAIR_GROUP_M 8
+#ifndef GB300_GROUP_PANEL_MB
+#define GB300_GROUP_PANEL_MB 32
 #endif
-constexpr int kPairGroupM = GB300_PAIR_GROUP_M;
-#ifndef GB300_L2_RESIDENT_MB
-#define GB300_L2_RESIDENT_MB 0
-#endif
-// When A is at most this large, the raster sweeps all row blocks for each column band so
-// that B streams through L2 once while A stays resident (0 disables the rule).
-constexpr int64_t kL2ResidentBytes = static_cast<int64_t>(GB300_L2_RESIDENT_MB) << 20;
+// Raster group size: as many row blocks as keep the group's panel of A (rows x K) within
+// this many bytes, so that the panel stays in L2 while the group sweeps all of B's column
+// blocks; B then streams from DRAM once per group (at least kMinGroup row blocks).
+constexpr int64_t kGroupPanelBytes = static_cast<int64_t>(GB300_GROUP_PANEL_MB) << 20;
+constexpr int kMinGroup = 4;
 
-int raster_group(int m_blocks, int64_t a_bytes, int default_group)
+int raster_group(int m_blocks, int rows_per_block, int K)
 {
-    if (kL2ResidentBytes > 0 && a_bytes <= kL2ResidentBytes)
-        return m_blocks;
-    return default_group;
+    const int64_t panel = static_cast<int64_t>(rows_per_block) * (K > 0 ? K : 1) * 2;
+    const int64_t g = kGroupPanelBytes / panel;
+    return static_cast<int>(std::max<int64_t>(kMinGroup, std::min<int64_t>(m_blocks, g)));
 }
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int kSoftmaxMaxN = 256;   // one tile spans the whole output row
 // gemm_run_host splits M into at most this many chunks whose uploads, GEMMs and downloads
 // overlap; outputs smaller than kHostChunkMinBytes are not split.
 constexpr int kHostChunksMax = 8;
@@ -132,12 +131,14 @@ int check_args(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, co
         return GEMM_ERR_ARG;
     if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
         return GEMM_ERR_ARG;
-    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_RELU)
+    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_SOFTMAX)
         return GEMM_ERR_ARG;
     if (M == 0 || N == 0)
         return GEMM_OK;
     if (!C || (K > 0 && (!A || !B)))
         return GEMM_ERR_ARG;
+    if (epilogue == GEMM_EPI_SOFTMAX && (N > kSoftmaxMaxN || Cfg::EPI_COL_GROUPS != 1))
+        return GEMM_ERR_ARG;   // the fused softmax needs whole rows inside one tile and one warp
     if (N % 8 != 0 || K % 8 != 0)
         return GEMM_ERR_ALIGN;
     if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B))) || (bias && !aligned16(bias)))
@@ -149,17 +150,18 @@ int check_args(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, co
     return GEMM_OK;
 }
 
-// 2-D FP16 tensor map over a row-major [outer x inner] matrix, 128-byte swizzled boxes of
-// box_inner x box_outer elements; out-of-range elements read as zero.
+// 2-D FP16 tensor map over a row-major [outer x inner] matrix with boxes of
+// box_inner x box_outer elements (swizzled as given); loads read out-of-range elements as
+// zero, stores skip them.
 bool encode_2d(gemm_ctx *ctx, CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
-               uint32_t box_inner, uint32_t box_outer)
+               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {inner * 2};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims,
-                                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -167,8 +169,9 @@ bool encode_2d(gemm_ctx *ctx, CUtensorMap *map, const void *ptr, uint64_t inner,
 // Launch with programmatic stream serialisation: the kernel may be scheduled while the
 // previous kernel in the stream is finishing and overlaps its own set-up with that tail;
 // it waits (griddepcontrol.wait) before touching global memory.
-void launch_pdl(void (*kernel)(CUtensorMap, CUtensorMap, gb300::GemmParams), int grid, int threads, int smem,
-                cudaStream_t stream, const CUtensorMap &ta, const CUtensorMap &tb, const gb300::GemmParams &p)
+void launch_pdl(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, gb300::GemmParams), int grid, int threads,
+                int smem, cudaStream_t stream, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                const gb300::GemmParams &p)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -180,13 +183,13 @@ void launch_pdl(void (*kernel)(CUtensorMap, CUtensorMap, gb300::GemmParams), int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaLaunchKernelEx(&cfg, kernel, ta, tb, p);
+    cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p);
 }
 
 int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, const void *bias, void *C,
            int epilogue, cudaStream_t stream)
 {
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tc;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
     if (K > 0) {
@@ -194,6 +197,10 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
             !encode_2d(ctx, &tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), Cfg::B_BOX_N, Cfg::BK))
             return GEMM_ERR_LAUNCH;
     }
+    // C is written by TMA in 32 x 32 boxes staged with the 64-byte swizzle
+    if (!encode_2d(ctx, &tc, C, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B))
+        return GEMM_ERR_LAUNCH;
     gb300::GemmParams p;
     p.M = M;
     p.N = N;
@@ -217,17 +224,17 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
         p.m_blocks = (M + PairCfg::BM - 1) / PairCfg::BM;
         p.n_blocks = (N + PairCfg::BN - 1) / PairCfg::BN;
         p.num_tiles = p.m_blocks * p.n_blocks;
-        p.group_m = raster_group(p.m_blocks, static_cast<int64_t>(M) * K * 2, kPairGroupM);
+        p.group_m = raster_group(p.m_blocks, PairCfg::BM, K);
         const int grid = 2 * std::min(p.num_tiles, ctx->max_clusters);
         launch_pdl(gb300::gemm_tcgen05_pair_kernel<PairCfg>, grid, PairCfg::NUM_THREADS, PairCfg::SMEM_BYTES, stream,
-                   ta, tb, p);
+                   ta, tb, tc, p);
     } else {
         p.m_blocks = (M + Cfg::BM - 1) / Cfg::BM;
         p.n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
         p.num_tiles = p.m_blocks * p.n_blocks;
-        p.group_m = raster_group(p.m_blocks, static_cast<int64_t>(M) * K * 2, kGroupM);
+        p.group_m = raster_group(p.m_blocks, Cfg::BM, K);
         const int grid = std::min(p.num_tiles, ctx->num_sms);
-        launch_pdl(gb300::gemm_tcgen05_kernel<Cfg>, grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream, ta, tb, p);
+        launch_pdl(gb300::gemm_tcgen05_kernel<Cfg>, grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -474,6 +481,38 @@ const char *gemm_status_string(int status)
 int gemm_num_sms(gemm_ctx *ctx) { return ctx ? ctx->num_sms : 0; }
 
 int gemm_num_pairs(gemm_ctx *ctx) { return ctx ? ctx->max_clusters : 0; }
+
+int gemm_row_softmax(gemm_ctx *ctx, int64_t rows, int64_t cols, const void *X, void *Y, void *stream)
+{
+    if (!ctx || rows < 0 || cols < 0 || cols > INT32_MAX)
+        return GEMM_ERR_ARG;
+    if (rows == 0 || cols == 0)
+        return GEMM_OK;
+    if (!X || !Y)
+        return GEMM_ERR_ARG;
+    if (cols % 8 != 0 || !aligned16(X) || !aligned16(Y))
+        return GEMM_ERR_ALIGN;
+    const size_t bytes = static_cast<size_t>(rows) * static_cast<size_t>(cols) * 2;
+    if (X != Y && overlaps(X, bytes, Y, bytes))   // in place is fine, partial overlap is not
+        return GEMM_ERR_ARG;
+    if (!on_device(X, ctx->device) || !on_device(Y, ctx->device))
+        return GEMM_ERR_DEVICE;
+    DeviceGuard guard(ctx->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int c = static_cast<int>(cols);
+    // one warp per row up to 2048 columns (at most 8 vectors per lane), else a 256-thread block
+    if (cols <= 2048) {
+        const int64_t blocks = std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(ctx->num_sms) * 8);
+        gb300::row_softmax_kernel<32><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+            static_cast<const __half *>(X), static_cast<__half *>(Y), rows, c);
+    } else {
+        const int64_t blocks = std::min<int64_t>(rows, static_cast<int64_t>(ctx->num_sms) * 8);
+        gb300::row_softmax_kernel<256><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+            static_cast<const __half *>(X), static_cast<__half *>(Y), rows, c);
+    }
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+}
 
 int gemm_set_timeout_ns(gemm_ctx *ctx, uint64_t ns)
 {

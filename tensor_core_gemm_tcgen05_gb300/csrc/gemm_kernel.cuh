@@ -46,7 +46,12 @@ enum : uint32_t {
     ERR_TEARDOWN_DRAIN = 5,
 };
 
-enum : int { EPI_NONE = 0, EPI_GELU = 1, EPI_RELU = 2 };
+enum : int { EPI_NONE = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_SOFTMAX = 3 };
+
+// Output staging of one epilogue warp: two 32-row x 32-column FP16 boxes (2 KB each,
+// 64-byte swizzle) that alternate between being filled and being stored by TMA.
+constexpr int EPI_STORE_BOX_BYTES = 32 * 32 * 2;
+constexpr int EPI_STORE_WARP_BYTES = 2 * EPI_STORE_BOX_BYTES;
 enum : int { DEBUG_WITHHOLD_FIRST_LOAD = 1 };
 
 struct GemmParams {
@@ -83,7 +88,9 @@ struct KernelConfig {
     // after the ring: barriers, TMEM address, stop flag; then one BN-wide bias slice per
     // epilogue warp (FP16)
     static constexpr int BIAS_OFFSET = STAGES * STAGE_BYTES + ((NUM_BARS * 8 + 16 + 15) / 16) * 16;
-    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + BIAS_OFFSET + NUM_EPI_WARPS * BN * 2;
+    // then, 1024-aligned, two 32 x 32 FP16 output staging boxes per epilogue warp
+    static constexpr int STORE_OFFSET = ((BIAS_OFFSET + NUM_EPI_WARPS * BN * 2 + 1023) / 1024) * 1024;
+    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES;
 
     static_assert(BM == 128, "one CTA, M = 128: TMEM lane i holds tile row i");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
@@ -224,11 +231,12 @@ __device__ __forceinline__ uint4 bias_fetch(const GemmParams &p, int n_tile0, in
 }
 
 // One 32-column chunk of one accumulator row per thread: + bias (from this warp's staged
-// slice in shared memory), activation in FP32, FP32 -> FP16 (round to nearest even), four
-// 16-byte streaming stores (C is written once and never re-read). `row_ok` masks rows >= M;
-// column groups of 8 at or past N are skipped.
-__device__ __forceinline__ void epilogue_math_store(const GemmParams &p, const uint32_t (&r)[32], const uint4 *sbias,
-                                                    int n0, __half *crow, bool row_ok)
+// slice in shared memory), activation in FP32, FP32 -> FP16 (round to nearest even), and
+// the 64 bytes of the row into the warp's staging box `box` (32 rows x 64 bytes, laid out
+// with the 64-byte swizzle the TMA store expects: 16-byte piece i of row r sits at
+// r*64 + (i ^ ((r >> 1) & 3))*16, which also spreads a warp's writes over all banks).
+__device__ __forceinline__ void epilogue_math_stage(const GemmParams &p, const uint32_t (&r)[32], const uint4 *sbias,
+                                                    uint32_t box, int lane)
 {
     float v[32];
 #pragma unroll
@@ -256,36 +264,139 @@ __device__ __forceinline__ void epilogue_math_store(const GemmParams &p, const u
         for (int j = 0; j < 32; ++j)
             v[j] = fmaxf(v[j], 0.0f);
     }
-    if (row_ok) {
+    const uint32_t row_base = box + static_cast<uint32_t>(lane) * 64u;
+    const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (n0 + 8 * i < p.N) {
-                uint4 out;
-                __half2 h0 = __floats2half2_rn(v[8 * i + 0], v[8 * i + 1]);
-                __half2 h1 = __floats2half2_rn(v[8 * i + 2], v[8 * i + 3]);
-                __half2 h2 = __floats2half2_rn(v[8 * i + 4], v[8 * i + 5]);
-                __half2 h3 = __floats2half2_rn(v[8 * i + 6], v[8 * i + 7]);
-                out.x = *reinterpret_cast<uint32_t *>(&h0);
-                out.y = *reinterpret_cast<uint32_t *>(&h1);
-                out.z = *reinterpret_cast<uint32_t *>(&h2);
-                out.w = *reinterpret_cast<uint32_t *>(&h3);
-                __stcs(reinterpret_cast<uint4 *>(crow + n0 + 8 * i), out);
+    for (int i = 0; i < 4; ++i) {
+        uint4 out;
+        __half2 h0 = __floats2half2_rn(v[8 * i + 0], v[8 * i + 1]);
+        __half2 h1 = __floats2half2_rn(v[8 * i + 2], v[8 * i + 3]);
+        __half2 h2 = __floats2half2_rn(v[8 * i + 4], v[8 * i + 5]);
+        __half2 h3 = __floats2half2_rn(v[8 * i + 6], v[8 * i + 7]);
+        out.x = *reinterpret_cast<uint32_t *>(&h0);
+        out.y = *reinterpret_cast<uint32_t *>(&h1);
+        out.z = *reinterpret_cast<uint32_t *>(&h2);
+        out.w = *reinterpret_cast<uint32_t *>(&h3);
+        st_shared_v4(row_base + ((static_cast<uint32_t>(i) ^ sw) << 4), out);
+    }
+}
+
+// Row-softmax epilogue ("Designing High-Performance GPU Kernels with TileLang", spaxe.top:
+// softmax applied to each row of the GEMM result in the epilogue, no intermediate written to
+// global memory). Valid when the tile spans every column of C (N <= BN) and one warp owns all
+// columns of its 32 rows: then each thread holds one whole row of logits in its TMEM lane
+// and needs no other thread. Pass 1 reads the row chunk by chunk and keeps a running maximum
+// m and a sum s of exp(x - m) rescaled whenever m grows; pass 2 reads the row again from
+// TMEM and stores exp(x - m) / s (columns at or past N are left out of both passes).
+template <int CHUNKS>
+__device__ __forceinline__ void epilogue_softmax_tile(const GemmParams &p, uint32_t taddr, int n_first, int row0,
+                                                      const uint4 *sbias, const CUtensorMap *tmap_c,
+                                                      uint32_t stage, uint32_t &box_sel, int lane)
+{
+    constexpr float kL2e = 1.4426950408889634f;
+    const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
+    if (valid <= 0 || row0 >= p.M)
+        return;
+    const bool has_acc = p.num_kb > 0;
+    auto logits = [&](int c, float (&v)[32]) {
+        uint32_t r[32];
+        if (has_acc) {
+            tmem_ld_32x32b_x32(taddr + 32u * c, r);
+            tmem_ld_wait_regs(r);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                r[j] = 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            v[j] = __uint_as_float(r[j]);
+        if (sbias != nullptr) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 bv = sbias[4 * c + i];
+                const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(bh[e]);
+                    v[8 * i + 2 * e] += f.x;
+                    v[8 * i + 2 * e + 1] += f.y;
+                }
             }
         }
+        const int n0 = n_first + 32 * c;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (n0 + j >= p.N)
+                v[j] = -INFINITY;   // not a column of C
+    };
+    float m = -INFINITY, s = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < valid; ++c) {
+        float v[32];
+        logits(c, v);
+        float vm = v[0];
+#pragma unroll
+        for (int j = 1; j < 32; ++j)
+            vm = fmaxf(vm, v[j]);
+        const float mn = fmaxf(m, vm);
+        float add = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            add += exp2f((v[j] - mn) * kL2e);
+        s = s * exp2f((m - mn) * kL2e) + add;
+        m = mn;
+    }
+    const float inv = 1.0f / s;
+#pragma unroll 1
+    for (int c = 0; c < valid; ++c) {
+        float v[32];
+        logits(c, v);
+        const uint32_t box = stage + box_sel * EPI_STORE_BOX_BYTES;
+        if (lane == 0)
+            bulk_wait_group_read<1>();
+        __syncwarp();
+        const uint32_t row_base = box + static_cast<uint32_t>(lane) * 64u;
+        const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __half2 h = __floats2half2_rn(exp2f((v[8 * i + 2 * e] - m) * kL2e) * inv,
+                                              exp2f((v[8 * i + 2 * e + 1] - m) * kL2e) * inv);
+                w[e] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            st_shared_v4(row_base + ((static_cast<uint32_t>(i) ^ sw) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmap_c, box, n_first + 32 * c, row0, l2_policy_evict_first());
+            bulk_commit_group();
+        }
+        box_sel ^= 1u;
     }
 }
 
 // Epilogue of one warp for one tile, step 2 (accumulator ready): up to CHUNKS chunks of 32
-// columns starting at TMEM address `taddr` / output column `n_first`. The TMEM load of chunk
-// c+1 is in flight while chunk c is processed. Called by all 32 lanes together
-// (tcgen05.ld is warp-collective; the chunk count is the same for every lane).
+// columns starting at TMEM address `taddr` / output column `n_first`, for the 32 output rows
+// starting at `row0`. The TMEM load of chunk c+1 is in flight while chunk c is processed;
+// each finished 32 x 32 box goes out with one TMA store from the warp's two alternating
+// staging boxes (`stage`, toggled through `box_sel`), which clips rows >= M and
+// columns >= N. Called by all 32 lanes together (tcgen05.ld is warp-collective).
 template <int CHUNKS>
-__device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t taddr, int n_first, __half *crow,
-                                              bool row_ok, const uint4 *sbias)
+__device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t taddr, int n_first, int row0,
+                                              const uint4 *sbias, const CUtensorMap *tmap_c, uint32_t stage,
+                                              uint32_t &box_sel, int lane)
 {
-    const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
-    if (valid <= 0)
+    if (p.epilogue == EPI_SOFTMAX) {
+        epilogue_softmax_tile<CHUNKS>(p, taddr, n_first, row0, sbias, tmap_c, stage, box_sel, lane);
         return;
+    }
+    const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
+    if (valid <= 0 || row0 >= p.M)
+        return;   // nothing of this warp's part of the tile is inside C
     const bool has_acc = p.num_kb > 0;   // K = 0: the empty sum, no accumulator to read
     uint32_t ra[32], rb[32];
 #pragma unroll
@@ -293,6 +404,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t tadd
         ra[j] = 0u;
         rb[j] = 0u;
     }
+    auto finish_chunk = [&](const uint32_t(&r)[32], int c) {
+        const uint32_t box = stage + box_sel * EPI_STORE_BOX_BYTES;
+        if (lane == 0)
+            bulk_wait_group_read<1>();   // the store that last used this box has read it
+        __syncwarp();
+        epilogue_math_stage(p, r, sbias ? sbias + 4 * c : nullptr, box, lane);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmap_c, box, n_first + 32 * c, row0, l2_policy_evict_first());
+            bulk_commit_group();
+        }
+        box_sel ^= 1u;
+    };
     if (has_acc)
         tmem_ld_32x32b_x32(taddr, ra);
 #pragma unroll 1
@@ -302,22 +427,22 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t tadd
             if (c + 1 < valid)
                 tmem_ld_32x32b_x32(taddr + 32u * (c + 1), rb);
         }
-        epilogue_math_store(p, ra, sbias ? sbias + 4 * c : nullptr, n_first + 32 * c, crow, row_ok);
+        finish_chunk(ra, c);
         if (c + 1 < valid) {
             if (has_acc) {
                 tmem_ld_wait_regs(rb);
                 if (c + 2 < valid)
                     tmem_ld_32x32b_x32(taddr + 32u * (c + 2), ra);
             }
-            epilogue_math_store(p, rb, sbias ? sbias + 4 * (c + 1) : nullptr, n_first + 32 * (c + 1), crow, row_ok);
+            finish_chunk(rb, c + 1);
         }
     }
 }
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
-    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                        const __grid_constant__ CUtensorMap tmap_b, const GemmParams p)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                        const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
 {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr uint32_t IDESC = idesc_f16_f32<BM, BN>();
@@ -337,6 +462,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     uint4 *bias_stage = reinterpret_cast<uint4 *>(sp + Cfg::BIAS_OFFSET);
+    const uint32_t store_stage = base + Cfg::STORE_OFFSET;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -357,6 +483,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             tma_prefetch_desc(&tmap_a);
             tma_prefetch_desc(&tmap_b);
         }
+        tma_prefetch_desc(&tmap_c);
     }
     if (warp == 1) {
         tmem_alloc<1>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -470,6 +597,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         constexpr int CHUNKS = BN / 32 / Cfg::EPI_COL_GROUPS;   // 32-column chunks per warp
         const int c_begin = ((warp - 2) >> 2) * CHUNKS;
         uint4 *my_bias = bias_stage + (warp - 2) * (BN / 8);   // this warp's BN-wide bias slice
+        const uint32_t my_stage = store_stage + static_cast<uint32_t>(warp - 2) * EPI_STORE_WARP_BYTES;
+        uint32_t box_sel = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
@@ -487,11 +616,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 my_bias[lane] = bv;
                 __syncwarp();
             }
-            const int row = mb * BM + quarter * 32 + lane;
-            __half *crow = p.C + static_cast<int64_t>(row) * p.N;
             epilogue_tile<CHUNKS>(p, tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c_begin * 32),
-                                  nb * BN + c_begin * 32, crow, row < p.M,
-                                  p.bias != nullptr ? my_bias + c_begin * 4 : nullptr);
+                                  nb * BN + c_begin * 32, mb * BM + quarter * 32,
+                                  p.bias != nullptr ? my_bias + c_begin * 4 : nullptr, &tmap_c, my_stage, box_sel,
+                                  lane);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
@@ -501,6 +629,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0)
+            bulk_wait_group<0>();   // every output box of this warp has reached global memory
+        __syncwarp();
     }
 
     tc_fence_before_sync();

@@ -45,7 +45,8 @@ struct PairConfig {
     static constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int BIAS_OFFSET = STAGES * STAGE_BYTES + ((NUM_BARS * 8 + 16 + 15) / 16) * 16;
-    static constexpr int SMEM_BYTES = 1024 + BIAS_OFFSET + NUM_EPI_WARPS * BN * 2;
+    static constexpr int STORE_OFFSET = ((BIAS_OFFSET + NUM_EPI_WARPS * BN * 2 + 1023) / 1024) * 1024;
+    static constexpr int SMEM_BYTES = 1024 + STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES;
 
     static_assert(BN % 128 == 0 && BN >= 128 && BN <= 256, "UMMA N for M = 256, two 64-column boxes per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM alloc size");
@@ -88,8 +89,8 @@ __device__ __forceinline__ bool pair_wait(uint32_t bar, uint32_t parity, const P
 
 template <class Cfg>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
-    gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                             const __grid_constant__ CUtensorMap tmap_b, const GemmParams p)
+    gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                             const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
 {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr uint32_t IDESC = idesc_f16_f32<BM, BN>();
@@ -108,6 +109,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     uint4 *bias_stage = reinterpret_cast<uint4 *>(sp + Cfg::BIAS_OFFSET);
+    const uint32_t store_stage = base + Cfg::STORE_OFFSET;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -132,6 +134,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
             tma_prefetch_desc(&tmap_a);
             tma_prefetch_desc(&tmap_b);
         }
+        tma_prefetch_desc(&tmap_c);
     }
     __syncwarp();
     cluster_sync();   // both CTAs' barriers exist before any remote arrive or TMA byte count
@@ -255,6 +258,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
         constexpr int CHUNKS = BN / 32 / Cfg::EPI_COL_GROUPS;
         const int c_begin = ((warp - 2) >> 2) * CHUNKS;
         uint4 *my_bias = bias_stage + (warp - 2) * (BN / 8);
+        const uint32_t my_stage = store_stage + static_cast<uint32_t>(warp - 2) * EPI_STORE_WARP_BYTES;
+        uint32_t box_sel = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
@@ -272,11 +277,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
                 my_bias[lane] = bv;
                 __syncwarp();
             }
-            const int row = mb * BM + static_cast<int>(rank) * Cfg::CTA_BM + quarter * 32 + lane;
-            __half *crow = p.C + static_cast<int64_t>(row) * p.N;
             epilogue_tile<CHUNKS>(p, tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c_begin * 32),
-                                  nb * BN + c_begin * 32, crow, row < p.M,
-                                  p.bias != nullptr ? my_bias + c_begin * 4 : nullptr);
+                                  nb * BN + c_begin * 32, mb * BM + static_cast<int>(rank) * Cfg::CTA_BM + quarter * 32,
+                                  p.bias != nullptr ? my_bias + c_begin * 4 : nullptr, &tmap_c, my_stage, box_sel,
+                                  lane);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
@@ -286,6 +290,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0)
+            bulk_wait_group<0>();   // every output box of this warp has reached global memory
+        __syncwarp();
     }
 
     tc_fence_before_sync();

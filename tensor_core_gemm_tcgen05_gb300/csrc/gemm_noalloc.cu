@@ -107,14 +107,15 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 }
 
 bool encode_2d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *map, const void *ptr, uint64_t inner,
-               uint64_t outer, uint32_t box_inner, uint32_t box_outer)
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {inner * 2};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -127,8 +128,10 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
     // (kScratchNeed) is the same for every size and fits the array.
     if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
         return GEMM_ERR_ARG;
-    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_RELU)
+    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_SOFTMAX)
         return GEMM_ERR_ARG;
+    if (epilogue == GEMM_EPI_SOFTMAX && N > 256)
+        return GEMM_ERR_ARG;   // the fused softmax needs whole rows inside one tile
     if (M == 0 || N == 0)
         return GEMM_OK;
     if (!C || (K > 0 && (!A || !B)))
@@ -155,7 +158,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
         (bias && !on_device(bias, device)))
         return GEMM_ERR_DEVICE;
 
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tc;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
     if (K > 0) {
@@ -165,6 +168,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
                        NoAllocCfg::BK))
             return GEMM_ERR_LAUNCH;
     }
+    if (!encode_2d(s.encode, &tc, C, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B))
+        return GEMM_ERR_LAUNCH;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The array keeps the previous call's contents: the error word must start at zero.
     if (cudaMemsetAsync(s.scratch, 0, kScratchNeed, st) != cudaSuccess) {
@@ -179,7 +185,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
     p.n_blocks = (p.N + NoAllocCfg::BN - 1) / NoAllocCfg::BN;
     p.num_tiles = p.m_blocks * p.n_blocks;
     p.num_kb = (p.K + NoAllocCfg::BK - 1) / NoAllocCfg::BK;
-    p.group_m = kGroupM;
+    p.group_m = kGroupM;   // row blocks per raster group
     p.epilogue = epilogue;
     p.bias = static_cast<const __half *>(bias);
     p.C = static_cast<__half *>(C);
@@ -187,7 +193,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
     p.timeout_ns = kTimeoutNs;
     p.debug = 0;
     const int grid = p.num_tiles < s.num_sms ? p.num_tiles : s.num_sms;
-    gb300::gemm_tcgen05_kernel<NoAllocCfg><<<grid, NoAllocCfg::NUM_THREADS, NoAllocCfg::SMEM_BYTES, st>>>(ta, tb, p);
+    gb300::gemm_tcgen05_kernel<NoAllocCfg><<<grid, NoAllocCfg::NUM_THREADS, NoAllocCfg::SMEM_BYTES, st>>>(ta, tb, tc, p);
     if (cudaGetLastError() != cudaSuccess)
         return GEMM_ERR_LAUNCH;
     return GEMM_OK;

@@ -24,8 +24,8 @@ import math
 import torch
 
 # Epilogue codes of the C ABI (bias is applied whenever a bias vector is passed).
-EPI_NONE, EPI_GELU, EPI_RELU = 0, 1, 2
-EPILOGUES = {"none": EPI_NONE, "gelu": EPI_GELU, "relu": EPI_RELU}
+EPI_NONE, EPI_GELU, EPI_RELU, EPI_SOFTMAX = 0, 1, 2, 3
+EPILOGUES = {"none": EPI_NONE, "gelu": EPI_GELU, "relu": EPI_RELU, "softmax": EPI_SOFTMAX}
 
 SEED_A, SEED_B, SEED_BIAS, SEED_ROWS = 1, 2, 3, 1234
 
@@ -38,7 +38,7 @@ class Workload:
     M: int
     N: int
     K: int
-    epilogue: str = "none"          # "none" | "gelu" | "relu"
+    epilogue: str = "none"          # "none" | "gelu" | "relu" | "softmax"
     bias: bool = False
     a_dist: str = "uniform"         # "uniform": U[-1,1]; "normal": N(0,1)
     b_dist: str = "uniform"         # "uniform": U[-1,1]; "normal_inv_k": N(0,1/K)
@@ -79,6 +79,11 @@ WORKLOADS: dict[str, Workload] = {
         Workload("mlp_up_8200x4096x16384_none", 8200, 16384, 4096, "none", False,
                  a_dist="normal", b_dist="normal_inv_k", bias_range=0.1,
                  sample_rows=512, include_last=8),
+        # GEMM with the row-softmax epilogue, shaped like attention scores: 262144 query rows
+        # (e.g. 128 heads x 2048 tokens) against 256 keys of dimension 128; queries N(0,1),
+        # keys N(0,1/K) so the logits are about N(0,1).
+        Workload("scores_262144x256x128_softmax", 262144, 256, 128, "softmax", False,
+                 a_dist="normal", b_dist="normal_inv_k", sample_rows=512, include_last=8),
     ]
 }
 

@@ -175,6 +175,47 @@ def test_activation_accuracy_on_every_fp16_input(ctx):
             assert not bad.any(), (bias[np.nonzero(bad[0])[0][:10]], err[bad][:10])
 
 
+@pytest.mark.parametrize("shape", [(300, 256, 128), (129, 200, 64), (1000, 8, 512), (64, 64, 4096),
+                                   (4104, 256, 128), (5, 136, 8)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_softmax_epilogue(kctx, shape, with_bias):
+    """GEMM with the fused row softmax: within one FP16 ulp of the oracle's softmax of the
+    FP64 logits (the GPU's logits are FP32 sums; their error, about 1e-6 relative, moves a
+    probability by far less than an FP16 ulp)."""
+    M, N, K = shape
+    A = inputs.random_fp16((M, K), 6000 + M, "normal")
+    B = inputs.random_fp16((K, N), 6100 + N, "normal_inv_k", k=K)
+    bias = inputs.random_fp16((N,), 6200 + N) if with_bias else None
+    C = run_guarded(kctx, A, B, bias, g.EPI_SOFTMAX).numpy()
+    ref = oracle_ref(A, B, bias, g.EPI_SOFTMAX)
+    ulp = np.maximum(np.spacing(np.abs(ref)).astype(np.float64), 2.0 ** -24)
+    err = np.abs(C.astype(np.float64) - ref.astype(np.float64))
+    assert np.all(np.isfinite(C.astype(np.float64)))
+    assert np.all(err <= ulp), (shape, float(err.max()), int((err > ulp).sum()))
+    assert np.all(np.abs(C.astype(np.float64).sum(axis=1) - 1) <= N * 2.0 ** -11)
+
+
+def test_softmax_epilogue_limits(ctx):
+    dev = torch.device("cuda:0")
+    A = torch.zeros(16, 64, dtype=torch.float16, device=dev)
+    B = torch.zeros(64, 264, dtype=torch.float16, device=dev)
+    C = torch.zeros(16, 264, dtype=torch.float16, device=dev)
+    with pytest.raises(g.GemmError) as e:      # the row does not fit one tile
+        g.gemm(ctx, A, B, None, g.EPI_SOFTMAX, out=C)
+    assert e.value.status == g.GEMM_ERR_ARG
+    # K = 0: softmax of the bias row; all-zero logits give 1/N everywhere
+    bias = inputs.random_fp16((256,), 99).to(dev)
+    C2 = torch.empty(3, 256, dtype=torch.float16, device=dev)
+    g.gemm_run(ctx, 3, 256, 0, None, None, bias, C2, g.EPI_SOFTMAX)
+    C3 = torch.empty(3, 256, dtype=torch.float16, device=dev)
+    g.gemm_run(ctx, 3, 256, 0, None, None, None, C3, g.EPI_SOFTMAX)
+    torch.cuda.synchronize()
+    ref, _ = oracle.softmax_rows(bias.cpu()[None, :].repeat(3, 1))
+    ulp = np.maximum(np.spacing(np.abs(ref)).astype(np.float64), 2.0 ** -24)
+    assert np.all(np.abs(C2.cpu().numpy().astype(np.float64) - ref.astype(np.float64)) <= ulp)
+    assert torch.all(C3 == 1.0 / 256)
+
+
 def test_empty_m_or_n_is_a_no_op(ctx):
     dev = torch.device("cuda:0")
     C = torch.full((4, 8), 3.0, dtype=torch.float16, device=dev)
@@ -223,7 +264,7 @@ def test_bad_arguments_are_rejected_before_launch(ctx):
     assert rc() == g.GEMM_OK
     assert rc(M=-1) == g.GEMM_ERR_ARG
     assert rc(K=2 ** 31) == g.GEMM_ERR_ARG
-    assert rc(epi=3) == g.GEMM_ERR_ARG
+    assert rc(epi=4) == g.GEMM_ERR_ARG
     assert rc(a=None) == g.GEMM_ERR_ARG
     assert rc(c=None) == g.GEMM_ERR_ARG
     assert rc(N=60) == g.GEMM_ERR_ALIGN

@@ -145,9 +145,10 @@ def test_relu_and_identity():
 # ---- the product -----------------------------------------------------------------------
 
 def test_textbook_examples(golden_dir):
-    acts = {"none": oracle.ACT_NONE, "gelu": oracle.ACT_GELU, "relu": oracle.ACT_RELU}
+    acts = {"none": oracle.ACT_NONE, "gelu": oracle.ACT_GELU, "relu": oracle.ACT_RELU,
+            "softmax": oracle.ACT_SOFTMAX}
     cases = _read_textbook(os.path.join(golden_dir, "gemm_textbook.txt"))
-    assert len(cases) >= 6
+    assert len(cases) >= 8
     for c in cases:
         A = np.array(c["A"], dtype=np.float16).reshape(c["M"], c["K"])
         B = np.array(c["B"], dtype=np.float16).reshape(c["K"], c["N"])
@@ -297,3 +298,79 @@ def test_inputs_are_seeded_and_fp16():
     rows = inputs.sample_rows(mlp.M, mlp.sample_rows, include_last=mlp.include_last)
     assert rows.numel() == 512 and rows.unique().numel() == 512
     assert rows[-8:].tolist() == list(range(8192, 8200))
+
+
+# ---- row-wise softmax ------------------------------------------------------------------
+
+def test_softmax_textbook_examples(golden_dir):
+    n = 0
+    for line in open(os.path.join(golden_dir, "softmax_textbook.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        xs, ys = line.split("|")
+        x = np.array([float(v) for v in xs.split()], dtype=np.float16)[None, :]
+        want = np.array([float(v) for v in ys.split()])
+        got, f64 = oracle.softmax_rows(x, want_f64=True)
+        # x is rounded to FP16 first (ln 3 is not exact in FP16); allow that shift
+        assert np.allclose(f64[0], want, rtol=0, atol=2e-4 if "1.0986" in xs else 1e-9), (line, f64)
+        assert np.array_equal(got[0].view(np.uint16), f64[0].astype(np.float16).view(np.uint16))
+        n += 1
+    assert n == 4
+
+
+def test_softmax_invariants():
+    rng = np.random.default_rng(3)
+    x = (np.round(rng.uniform(-4, 4, (37, 50)) * 64) / 64).astype(np.float16)
+    y, f64 = oracle.softmax_rows(x, want_f64=True)
+    assert np.allclose(f64.sum(axis=1), 1.0, rtol=0, atol=1e-13)
+    assert np.all(f64 > 0)
+    # adding a constant to a row changes nothing (x + 8 is exact in FP16 here)
+    y2, f2 = oracle.softmax_rows((x.astype(np.float64) + 8.0).astype(np.float16), want_f64=True)
+    assert np.array_equal(f64, f2) and np.array_equal(y.view(np.uint16), y2.view(np.uint16))
+    # the largest entry of a row gets the largest probability; order is preserved
+    assert np.array_equal(np.argmax(f64, axis=1), np.argmax(x.astype(np.float64), axis=1))
+    # a uniform row is 1/n everywhere
+    u, fu = oracle.softmax_rows(np.full((2, 16), 3.5, np.float16), want_f64=True)
+    assert np.all(fu == 1.0 / 16)
+
+
+def test_softmax_against_scipy_and_brute_force():
+    from scipy.special import softmax as sp_softmax
+    x = inputs.random_fp16((64, 300), 91, scale=1.0).numpy() * np.float16(6)
+    _, f64 = oracle.softmax_rows(x, want_f64=True)
+    assert np.allclose(f64, sp_softmax(x.astype(np.float64), axis=1), rtol=1e-13, atol=1e-300)
+    small = x[:3, :5]
+    _, fs = oracle.softmax_rows(small, want_f64=True)
+    for r in range(3):
+        e = [math.exp(float(v)) for v in small[r].astype(np.float64)]
+        s = sum(e)
+        assert np.allclose(fs[r], [v / s for v in e], rtol=1e-14, atol=0)
+
+
+def test_softmax_extremes_and_empty():
+    x = np.full((1, 8), -11.0, np.float16)
+    x[0, 3] = 11.0
+    y, f64 = oracle.softmax_rows(x, want_f64=True)
+    assert abs(f64[0, 3] - 1.0) < 1e-8 and np.all(f64[0, np.arange(8) != 3] < 3e-10)
+    assert float(y[0, 3]) == 1.0
+    y0, _ = oracle.softmax_rows(np.zeros((0, 5), np.float16))
+    assert y0.shape == (0, 5)
+
+
+def test_gemm_softmax_epilogue_against_numpy():
+    from scipy.special import softmax as sp_softmax
+    for (M, N, K) in [(37, 8, 5), (64, 200, 96), (130, 256, 300)]:
+        A = inputs.random_fp16((M, K), 51 + N).numpy()
+        B = inputs.random_fp16((K, N), 52 + N).numpy()
+        bias = inputs.random_fp16((N,), 53 + N).numpy()
+        logits = A.astype(np.float64) @ B.astype(np.float64) + bias.astype(np.float64)
+        got, f64, _ = oracle.gemm(A, B, bias, oracle.ACT_SOFTMAX, want_f64=True)
+        assert np.allclose(f64, sp_softmax(logits, axis=1), rtol=1e-12, atol=1e-300)
+        assert np.allclose(f64.sum(axis=1), 1.0, atol=1e-13)
+        # the logits are not rounded to FP16 before the softmax: compare with the rounded path
+        rounded, _ = oracle.softmax_rows(logits.astype(np.float16))
+        assert np.abs(rounded.astype(np.float64) - got.astype(np.float64)).max() < 0.05
+        # row sampling agrees with the full computation
+        rows = [0, M // 2, M - 1]
+        part, _, _ = oracle.gemm(A, B, bias, oracle.ACT_SOFTMAX, rows=rows)
+        assert np.array_equal(part.view(np.uint16), got[rows].view(np.uint16))
