@@ -53,6 +53,11 @@ def _load():
             lib.oracle_softmax_rows.restype = ctypes.c_int
             lib.oracle_softmax_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.oracle_attention_rows.restype = ctypes.c_int
+            lib.oracle_attention_rows.argtypes = [
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
+                ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.oracle_gemm_rows.restype = ctypes.c_int
             lib.oracle_gemm_rows.argtypes = [
                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
@@ -139,3 +144,29 @@ def softmax_rows(X, threads: int = 0, want_f64: bool = False):
     if rc != 0:
         raise RuntimeError(f"oracle_softmax_rows failed with code {rc}")
     return y.view(np.float16), yd
+
+
+def attention(Q, K, V, scale: float, causal: bool, rows=None, threads: int = 0, want_f64: bool = False):
+    """Oracle attention output ``softmax(scale * Q K^T [+ causal mask]) V`` per head.
+
+    Q is [H, Sq, D], K and V are [H, Sk, D] (FP16). ``rows`` is a list of (head, query)
+    pairs (all of them when None). Returns ``(out fp16 [nrows, D], out_f64 or None)``.
+    """
+    q, k, v = _u16(Q), _u16(K), _u16(V)
+    if q.ndim != 3 or k.ndim != 3 or v.shape != k.shape or q.shape[0] != k.shape[0] or q.shape[2] != k.shape[2]:
+        raise ValueError("Q [H,Sq,D], K and V [H,Sk,D] expected")
+    H, Sq, D = q.shape
+    Sk = k.shape[1]
+    if rows is None:
+        rows = [(h, i) for h in range(H) for i in range(Sq)]
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 2))
+    n = r.shape[0]
+    out = np.empty((n, D), dtype=np.uint16)
+    outd = np.empty((n, D), dtype=np.float64) if want_f64 else None
+    rc = _load().oracle_attention_rows(H, Sq, Sk, D, q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                       float(scale), int(bool(causal)), r.ctypes.data, n,
+                                       out.ctypes.data, None if outd is None else outd.ctypes.data,
+                                       int(threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention_rows failed with code {rc}")
+    return out.view(np.float16), outd

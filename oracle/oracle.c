@@ -27,7 +27,8 @@
  *
  * The file also holds the row-wise softmax of the same tutorial (oracle_softmax_rows), and
  * the GEMM with a row-softmax epilogue (act = 3): softmax over each row of A*B + bias, the
- * logits kept in double (never rounded to FP16).
+ * logits kept in double (never rounded to FP16), and the attention forward result
+ * (oracle_attention_rows) that the FlashAttention kernel computes.
  *
  * Parity pins (tests/test_oracle.py): exhaustive FP16 decoding and RNE encoding against
  * numpy; a textbook worked example; identity and all-ones products; brute-force loops on
@@ -183,6 +184,114 @@ int oracle_softmax_rows(int64_t rows, int64_t cols, const uint16_t *X, uint16_t 
     free(th);
     free(jobs);
     return 0;
+}
+
+/* ---- attention forward ---------------------------------------------------------------------
+ * For every head h and query row i (FlashAttention's forward result, computed the plain way:
+ * "TileLang ..." (pro.edgex.exchange), FlashAttention paragraph: query, key and value tiles,
+ * online softmax; the result is ordinary attention):
+ *   s_j = scale * sum_d q[h][i][d] * k[h][j][d]            for keys j (j <= i when causal)
+ *   O[h][i][d] = fp16_rne( sum_j exp(s_j - max_j s_j) * v[h][j][d] / sum_j exp(s_j - max s) )
+ * Q is [H][Sq][D], K and V are [H][Sk][D], O is [H][Sq][D], all FP16 row-major, widened
+ * exactly to double; everything in double. Causal: key j is visible to query i iff j <= i. */
+typedef struct {
+    int64_t H, Sq, Sk, D;
+    const uint16_t *Q, *K, *V;
+    double scale;
+    int causal;
+    const int64_t *rows;   /* (head, query) pairs: rows[2t], rows[2t+1] */
+    int64_t nrows;
+    uint16_t *out;         /* nrows x D */
+    double *outd;
+    int tid, nthreads, failed;
+} attn_job_t;
+
+static void *attn_worker(void *arg)
+{
+    attn_job_t *j = (attn_job_t *)arg;
+    const int64_t Sk = j->Sk, D = j->D;
+    double *s = (double *)malloc((size_t)(Sk > 0 ? Sk : 1) * sizeof(double));
+    double *o = (double *)malloc((size_t)(D > 0 ? D : 1) * sizeof(double));
+    if (!s || !o) {
+        j->failed = 1;
+        free(s);
+        free(o);
+        return NULL;
+    }
+    for (int64_t t = j->tid; t < j->nrows; t += j->nthreads) {
+        const int64_t h = j->rows[2 * t], i = j->rows[2 * t + 1];
+        const uint16_t *q = j->Q + (h * j->Sq + i) * D;
+        const int64_t nk = j->causal ? (i + 1 < Sk ? i + 1 : Sk) : Sk;
+        double mx = -INFINITY;
+        for (int64_t k = 0; k < nk; ++k) {
+            const uint16_t *kr = j->K + (h * Sk + k) * D;
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d)
+                acc += oracle_half_to_double(q[d]) * oracle_half_to_double(kr[d]);
+            s[k] = j->scale * acc;
+            if (s[k] > mx)
+                mx = s[k];
+        }
+        double sum = 0.0;
+        for (int64_t k = 0; k < nk; ++k) {
+            s[k] = exp(s[k] - mx);
+            sum += s[k];
+        }
+        for (int64_t d = 0; d < D; ++d)
+            o[d] = 0.0;
+        for (int64_t k = 0; k < nk; ++k) {
+            const uint16_t *vr = j->V + (h * Sk + k) * D;
+            for (int64_t d = 0; d < D; ++d)
+                o[d] += s[k] * oracle_half_to_double(vr[d]);
+        }
+        for (int64_t d = 0; d < D; ++d) {
+            const double y = nk > 0 ? o[d] / sum : 0.0;
+            if (j->outd)
+                j->outd[t * D + d] = y;
+            j->out[t * D + d] = oracle_double_to_half(y);
+        }
+    }
+    free(s);
+    free(o);
+    return NULL;
+}
+
+/* Attention output rows for the (head, query) pairs in `rows` (2 * nrows int64 values).
+ * Returns 0, -1 for bad arguments, -2 when memory runs out. */
+int oracle_attention_rows(int64_t H, int64_t Sq, int64_t Sk, int64_t D, const uint16_t *Q, const uint16_t *K,
+                          const uint16_t *V, double scale, int causal, const int64_t *rows, int64_t nrows,
+                          uint16_t *out, double *outd, int threads)
+{
+    if (H < 0 || Sq < 0 || Sk < 0 || D < 0 || nrows < 0 || !rows || !out || !Q || !K || !V)
+        return -1;
+    for (int64_t t = 0; t < nrows; ++t)
+        if (rows[2 * t] < 0 || rows[2 * t] >= H || rows[2 * t + 1] < 0 || rows[2 * t + 1] >= Sq)
+            return -1;
+    if (nrows == 0)
+        return 0;
+    int T = threads > 0 ? threads : oracle_default_threads();
+    if (T > nrows)
+        T = (int)nrows;
+    pthread_t *th = (pthread_t *)malloc((size_t)T * sizeof(pthread_t));
+    attn_job_t *jobs = (attn_job_t *)calloc((size_t)T, sizeof(attn_job_t));
+    if (!th || !jobs) {
+        free(th);
+        free(jobs);
+        return -2;
+    }
+    for (int t = 0; t < T; ++t) {
+        jobs[t] = (attn_job_t){H, Sq, Sk, D, Q, K, V, scale, causal, rows, nrows, out, outd, t, T, 0};
+        pthread_create(&th[t], NULL, attn_worker, &jobs[t]);
+    }
+    int rc = 0;
+    for (int t = 0; t < T; ++t) {
+        pthread_join(th[t], NULL);
+        if (jobs[t].failed)
+            rc = -2;
+    }
+    free(th);
+    free(jobs);
+    return rc;
 }
 
 /* ---- the GEMM --------------------------------------------------------------------------- */

@@ -374,3 +374,66 @@ def test_gemm_softmax_epilogue_against_numpy():
         rows = [0, M // 2, M - 1]
         part, _, _ = oracle.gemm(A, B, bias, oracle.ACT_SOFTMAX, rows=rows)
         assert np.array_equal(part.view(np.uint16), got[rows].view(np.uint16))
+
+
+# ---- attention forward -------------------------------------------------------------------
+
+def _np_attention(Q, K, V, scale, causal):
+    from scipy.special import softmax as sp_softmax
+    q, k, v = (t.astype(np.float64) for t in (Q, K, V))
+    s = scale * np.einsum("hid,hjd->hij", q, k)
+    if causal:
+        Sq, Sk = s.shape[1], s.shape[2]
+        s = np.where(np.arange(Sk)[None, None, :] <= np.arange(Sq)[None, :, None], s, -np.inf)
+    return np.einsum("hij,hjd->hid", sp_softmax(s, axis=2), v)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_against_scipy_composition(causal):
+    rng = np.random.default_rng(5 + causal)
+    H, S, D = 3, 67, 32
+    Q, K, V = (rng.normal(0, 1, (H, S, D)).astype(np.float16) for _ in range(3))
+    out, f64 = oracle.attention(Q, K, V, 1 / np.sqrt(D), causal, want_f64=True)
+    want = _np_attention(Q, K, V, 1 / np.sqrt(D), causal).reshape(H * S, D)
+    assert np.allclose(f64, want, rtol=1e-12, atol=1e-13)
+    assert np.array_equal(out.view(np.uint16), f64.astype(np.float16).view(np.uint16))
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(9)
+    H, S, D = 2, 9, 8
+    V = rng.uniform(-1, 1, (H, S, D)).astype(np.float16)
+    K = rng.uniform(-1, 1, (H, S, D)).astype(np.float16)
+    # one key: the output is that key's value row, exactly
+    out, f = oracle.attention(rng.normal(0, 1, (H, 1, D)).astype(np.float16), K[:, :1], V[:, :1], 0.3, False,
+                              want_f64=True)
+    assert np.array_equal(f, V[:, 0].astype(np.float64))
+    # causal: the first query sees only the first key
+    Q = rng.normal(0, 1, (H, S, D)).astype(np.float16)
+    _, f = oracle.attention(Q, K, V, 0.3, True, rows=[(0, 0), (1, 0)], want_f64=True)
+    assert np.array_equal(f, V[:, 0].astype(np.float64))
+    # zero queries: every score is equal, so the output is the mean (causal: prefix mean)
+    Z = np.zeros((H, S, D), np.float16)
+    _, f = oracle.attention(Z, K, V, 0.3, False, want_f64=True)
+    assert np.allclose(f.reshape(H, S, D), V.astype(np.float64).mean(axis=1, keepdims=True).repeat(S, 1), atol=1e-15)
+    _, f = oracle.attention(Z, K, V, 0.3, True, want_f64=True)
+    pref = np.cumsum(V.astype(np.float64), axis=1) / np.arange(1, S + 1)[None, :, None]
+    assert np.allclose(f.reshape(H, S, D), pref, atol=1e-15)
+    # a very large scale makes the softmax one-hot on the best-matching key
+    _, f = oracle.attention(K, K, V, 200.0, False, rows=[(0, 4)], want_f64=True)
+    best = np.argmax(K[0].astype(np.float64) @ K[0, 4].astype(np.float64))
+    assert np.allclose(f[0], V[0, best].astype(np.float64), atol=1e-6)
+
+
+def test_attention_brute_force_tiny():
+    rng = np.random.default_rng(2)
+    H, S, D = 1, 4, 3
+    Q, K, V = (rng.uniform(-2, 2, (H, S, D)).astype(np.float16) for _ in range(3))
+    _, f = oracle.attention(Q, K, V, 0.7, True, want_f64=True)
+    for i in range(S):
+        s = [0.7 * sum(float(Q[0, i, d]) * float(K[0, j, d]) for d in range(D)) for j in range(i + 1)]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        for d in range(D):
+            want = sum(e[j] * float(V[0, j, d]) for j in range(i + 1)) / sum(e)
+            assert abs(f[i, d] - want) < 1e-14
