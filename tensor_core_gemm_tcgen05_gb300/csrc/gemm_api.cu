@@ -154,10 +154,11 @@ int check_args(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, co
 // box_inner x box_outer elements (swizzled as given); loads read out-of-range elements as
 // zero, stores skip them.
 bool encode_2d(gemm_ctx *ctx, CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
-               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
+               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+               uint64_t ld = 0 /* row stride in elements; 0: tightly packed */)
 {
     const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint64_t strides[1] = {(ld ? ld : inner) * 2};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims,
@@ -186,20 +187,23 @@ void launch_pdl(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, gb300::Gem
     cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p);
 }
 
+// ldb / ldc: row strides of B and C in elements (0: N, tightly packed); A is always packed.
+// gemm_run_host uses them to run column bands of a larger B and C.
 int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, const void *bias, void *C,
-           int epilogue, cudaStream_t stream)
+           int epilogue, cudaStream_t stream, int64_t ldb = 0, int64_t ldc = 0)
 {
     CUtensorMap ta, tb, tc;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
     if (K > 0) {
         if (!encode_2d(ctx, &ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), Cfg::BK, Cfg::BM) ||
-            !encode_2d(ctx, &tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), Cfg::B_BOX_N, Cfg::BK))
+            !encode_2d(ctx, &tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), Cfg::B_BOX_N, Cfg::BK,
+                       CU_TENSOR_MAP_SWIZZLE_128B, static_cast<uint64_t>(ldb)))
             return GEMM_ERR_LAUNCH;
     }
     // C is written by TMA in 32 x 32 boxes staged with the 64-byte swizzle
     if (!encode_2d(ctx, &tc, C, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 32, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B))
+                   CU_TENSOR_MAP_SWIZZLE_64B, static_cast<uint64_t>(ldc)))
         return GEMM_ERR_LAUNCH;
     gb300::GemmParams p;
     p.M = M;
@@ -373,41 +377,74 @@ int gemm_run_host(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A,
     char *dbias = bias ? base + round256(a_b) + round256(b_b) : nullptr;
     char *dC = base + round256(a_b) + round256(b_b) + round256(bias_b);
 
-    // Chunks of whole 256-row tiles: the upload of chunk i+1, the GEMM of chunk i and the
-    // download of chunk i-1 run at the same time (copy_in, s, copy_out). B and the bias go
-    // first, on s, since every chunk needs them.
-    int chunks = c_b < kHostChunkMinBytes ? 1 : 4;
-    int64_t rows = (M + chunks - 1) / chunks;
-    rows = (rows + 255) / 256 * 256;
-    chunks = static_cast<int>((M + rows - 1) / rows);
     if ((e = cudaEventRecord(ctx->ev_start, s)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(ctx->copy_in, ctx->ev_start, 0)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(ctx->copy_out, ctx->ev_start, 0)) != cudaSuccess)
         return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
-    if (b_b && (e = cudaMemcpyAsync(dB, B, b_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-        return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
     if (bias_b && (e = cudaMemcpyAsync(dbias, bias, bias_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
         return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
-    for (int i = 0; i < chunks; ++i) {
-        const int64_t r0 = i * rows, mi = std::min<int64_t>(rows, M - r0);
-        const size_t a_off = static_cast<size_t>(r0) * K * 2, c_off = static_cast<size_t>(r0) * N * 2;
-        const size_t a_len = static_cast<size_t>(mi) * K * 2, c_len = static_cast<size_t>(mi) * N * 2;
-        if (a_len && (e = cudaMemcpyAsync(dA + a_off, static_cast<const char *>(A) + a_off, a_len,
-                                          cudaMemcpyHostToDevice, ctx->copy_in)) != cudaSuccess)
+    // The output is produced in bands whose upload, GEMM and download overlap (copy_in, s,
+    // copy_out). The operand every band needs goes first, whole; the other one is cut into
+    // bands. Cutting C into column bands sends all of A first, cutting it into row bands
+    // all of B: whichever is smaller goes first, so the first band starts sooner. (The
+    // softmax epilogue needs whole rows, so it always uses row bands.)
+    const int parts = c_b < kHostChunkMinBytes ? 1 : 4;
+    const bool by_cols = parts > 1 && a_b < b_b && epilogue != GEMM_EPI_SOFTMAX;
+    if (by_cols) {
+        int64_t cols = (N + parts - 1) / parts;
+        cols = (cols + 255) / 256 * 256;   // whole 256-column tiles
+        const int bands = static_cast<int>((N + cols - 1) / cols);
+        if (a_b && (e = cudaMemcpyAsync(dA, A, a_b, cudaMemcpyHostToDevice, ctx->copy_in)) != cudaSuccess)
             return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
-        if ((e = cudaEventRecord(ctx->ev_in[i], ctx->copy_in)) != cudaSuccess ||
-            (e = cudaStreamWaitEvent(s, ctx->ev_in[i], 0)) != cudaSuccess)
+        const size_t pitch = static_cast<size_t>(N) * 2;
+        for (int j = 0; j < bands; ++j) {
+            const int64_t c0 = j * cols, nj = std::min<int64_t>(cols, N - c0);
+            const size_t off = static_cast<size_t>(c0) * 2, width = static_cast<size_t>(nj) * 2;
+            if (K > 0 && (e = cudaMemcpy2DAsync(dB + off, pitch, static_cast<const char *>(B) + off, pitch, width,
+                                                static_cast<size_t>(K), cudaMemcpyHostToDevice, ctx->copy_in)) !=
+                             cudaSuccess)
+                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+            if ((e = cudaEventRecord(ctx->ev_in[j], ctx->copy_in)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(s, ctx->ev_in[j], 0)) != cudaSuccess)
+                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+            rc = launch(ctx, static_cast<int>(M), static_cast<int>(nj), static_cast<int>(K), K ? dA : nullptr,
+                        K ? dB + off : nullptr, dbias ? dbias + off : nullptr, dC + off, epilogue, s, N, N);
+            if (rc != GEMM_OK)
+                return rc;
+            if ((e = cudaEventRecord(ctx->ev_mm[j], s)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(ctx->copy_out, ctx->ev_mm[j], 0)) != cudaSuccess)
+                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+            if ((e = cudaMemcpy2DAsync(static_cast<char *>(C) + off, pitch, dC + off, pitch, width,
+                                       static_cast<size_t>(M), cudaMemcpyDeviceToHost, ctx->copy_out)) != cudaSuccess)
+                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+        }
+    } else {
+        int64_t rows = (M + parts - 1) / parts;
+        rows = (rows + 255) / 256 * 256;   // whole 256-row tiles
+        const int chunks = static_cast<int>((M + rows - 1) / rows);
+        if (b_b && (e = cudaMemcpyAsync(dB, B, b_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
             return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
-        rc = launch(ctx, static_cast<int>(mi), static_cast<int>(N), static_cast<int>(K), K ? dA + a_off : nullptr,
-                    K ? dB : nullptr, dbias, dC + c_off, epilogue, s);
-        if (rc != GEMM_OK)
-            return rc;
-        if ((e = cudaEventRecord(ctx->ev_mm[i], s)) != cudaSuccess ||
-            (e = cudaStreamWaitEvent(ctx->copy_out, ctx->ev_mm[i], 0)) != cudaSuccess)
-            return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
-        if ((e = cudaMemcpyAsync(static_cast<char *>(C) + c_off, dC + c_off, c_len, cudaMemcpyDeviceToHost,
-                                 ctx->copy_out)) != cudaSuccess)
-            return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+        for (int i = 0; i < chunks; ++i) {
+            const int64_t r0 = i * rows, mi = std::min<int64_t>(rows, M - r0);
+            const size_t a_off = static_cast<size_t>(r0) * K * 2, c_off = static_cast<size_t>(r0) * N * 2;
+            const size_t a_len = static_cast<size_t>(mi) * K * 2, c_len = static_cast<size_t>(mi) * N * 2;
+            if (a_len && (e = cudaMemcpyAsync(dA + a_off, static_cast<const char *>(A) + a_off, a_len,
+                                              cudaMemcpyHostToDevice, ctx->copy_in)) != cudaSuccess)
+                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+            if ((e = cudaEventRecord(ctx->ev_in[i], ctx->copy_in)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(s, ctx->ev_in[i], 0)) != cudaSuccess)
+                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+            rc = launch(ctx, static_cast<int>(mi), static_cast<int>(N), static_cast<int>(K), K ? dA + a_off : nullptr,
+                        K ? dB : nullptr, dbias, dC + c_off, epilogue, s);
+            if (rc != GEMM_OK)
+                return rc;
+            if ((e = cudaEventRecord(ctx->ev_mm[i], s)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(ctx->copy_out, ctx->ev_mm[i], 0)) != cudaSuccess)
+                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+            if ((e = cudaMemcpyAsync(static_cast<char *>(C) + c_off, dC + c_off, c_len, cudaMemcpyDeviceToHost,
+                                     ctx->copy_out)) != cudaSuccess)
+                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+        }
     }
     if ((e = cudaEventRecord(ctx->ev_done, ctx->copy_out)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(s, ctx->ev_done, 0)) != cudaSuccess ||

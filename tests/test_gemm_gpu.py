@@ -332,6 +332,16 @@ def test_host_buffer_entry_point(ctx):
     rows = np.union1d(rows, [0, 1279, 1280, 2559, 2560, 3839, 3840])
     assert bool(torch.isfinite(C).all())
     assert_parity(C.numpy()[rows], oracle_ref(A, B, bias, g.EPI_GELU, rows=rows), "gemm_run_host chunked")
+    # A smaller than B: column bands of C (2304, 2304, 2304 and a ragged 1288 columns)
+    M, N, K = 2056, 8200, 512
+    A = inputs.random_fp16((M, K), 77).pin_memory()
+    B = inputs.random_fp16((K, N), 78).pin_memory()
+    bias = inputs.random_fp16((N,), 79).pin_memory()
+    C = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+    g.gemm_run_host(ctx, M, N, K, A, B, bias, C, g.EPI_RELU)
+    assert bool(torch.isfinite(C).all())
+    rows = inputs.sample_rows(M, 200, seed=9, include_last=4).numpy()
+    assert_parity(C.numpy()[rows], oracle_ref(A, B, bias, g.EPI_RELU, rows=rows), "gemm_run_host column bands")
 
 
 def test_side_stream_and_cuda_graph(ctx):
