@@ -299,6 +299,41 @@ def measure_fused_softmax(g, ctx, stream, device, peaks, steps=30):
         "tflops": round(w.flops / (out["fused"] * 1e-6) / 1e12, 1), "algorithmic_bytes_per_launch": w.bytes}}
 
 
+ATTN_SHAPE = (64, 4096)   # heads (e.g. batch 4 x 16 heads) and tokens, head dimension 128
+
+
+def measure_attention(g, ctx, stream, device, peaks, steps=10):
+    """FlashAttention forward (the last next-row): flops 4 * heads * S^2 * 128 (half of it
+    when causal), against the dense tensor peak."""
+    import math
+    import torch
+    from tensor_core_gemm_tcgen05_gb300 import inputs
+    H, S = ATTN_SHAPE
+    Q, K, V = (inputs.random_fp16((H, S, 128), 900 + i, "normal").to(device) for i in range(3))
+    O = torch.empty_like(Q)
+    out = {}
+    for causal in (False, True):
+        def fn():
+            g.gemm_attention_fwd(ctx, H, S, S, 128, Q, K, V, O, 1.0 / math.sqrt(128), causal, stream)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / steps * 1e3
+        flops = 4 * H * S * S * 128 * (0.5 if causal else 1.0)
+        tf = flops / (us * 1e-6) / 1e12
+        out[f"attention_fwd_{H}x{S}x128_{'causal' if causal else 'full'}"] = {
+            "us_per_launch": round(us, 1), "tflops": round(tf, 1), "bound": "tensor",
+            "pct_of_burst_peak": round(100 * tf / float(peaks["bf16_tflops"]), 2)}
+    return out
+
+
 def measure_e2e(g, ctx, w, host, stream, steps):
     """Same metric through gemm_run_host: pinned host inputs copied in, C copied out, every
     step inside the timed region (host wall clock around synchronous calls)."""
@@ -426,6 +461,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         side.update(measure_softmax(g, ctx, stream, device, peaks))
         side.update(measure_fused_softmax(g, ctx, stream, device, peaks))
+        side.update(measure_attention(g, ctx, stream, device, peaks))
 
     e2e = None if args.no_e2e else measure_e2e(g, ctx, w, host, stream, steps=max(3, min(args.steps, 10)))
     base = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, host)

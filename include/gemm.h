@@ -145,6 +145,25 @@ int gemm_num_pairs(gemm_ctx *ctx);
  * all -inf gives NaN). Asynchronous on `stream`; allocates nothing; one kernel launch. */
 int gemm_row_softmax(gemm_ctx *ctx, int64_t rows, int64_t cols, const void *X, void *Y, void *stream);
 
+/* FlashAttention forward: for every head h and query i,
+ *   O[h][i][:] = sum_j softmax_j(scale * Q[h][i][:] . K[h][j][:]) V[h][j][:],
+ * with j restricted to j <= i when `causal` is 1 ("TileLang ..." (pro.edgex.exchange),
+ * FlashAttention paragraph: query, key and value tiles, online softmax with running maxima,
+ * normalising sums and rescaling, without materialising the score matrix; "Designing
+ * High-Performance GPU Kernels with TileLang" (spaxe.top): causal and non-causal).
+ *   heads, seq_q, seq_k: 0 <= each <= 2^31 - 1; heads = 0 or seq_q = 0 is a no-op;
+ *               seq_k = 0 is an error. head_dim must be 128.
+ *   Q          : device pointer, [heads][seq_q][128] FP16, contiguous, 16-byte aligned.
+ *   K, V       : device pointers, [heads][seq_k][128] FP16, contiguous, 16-byte aligned.
+ *   O          : device pointer, [heads][seq_q][128] FP16, written; must not overlap Q/K/V.
+ *   scale      : multiplies Q.K (commonly 1/sqrt(128)); causal: 0 or 1.
+ * FP32 scores and accumulation in Tensor Memory, probabilities rounded to FP16 for the P V
+ * product, one RNE rounding of O. Asynchronous on `stream`; allocates nothing; one kernel
+ * launch. In-kernel waits report through gemm_last_device_error like the GEMM. */
+int gemm_attention_fwd(gemm_ctx *ctx, int64_t heads, int64_t seq_q, int64_t seq_k, int64_t head_dim,
+                       const void *Q, const void *K, const void *V, void *O, float scale, int causal,
+                       void *stream);
+
 /* Test hooks (no effect on results when left at their defaults).
  *   gemm_set_timeout_ns: the limit of every in-kernel wait (default 2e9 ns; values below
  *     1e6 are raised to 1e6).

@@ -42,7 +42,7 @@ EXPORTS = (
     "gemm_create", "gemm_run", "gemm_run_host", "gemm_last_device_error",
     "gemm_last_cuda_error", "gemm_destroy", "gemm_status_string", "gemm_num_sms",
     "gemm_set_timeout_ns", "gemm_set_debug", "gemm_run_noalloc", "gemm_num_pairs",
-    "gemm_row_softmax",
+    "gemm_row_softmax", "gemm_attention_fwd",
 )
 GEMM_NOALLOC_SCRATCH_BYTES = 256
 
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
             L.gemm_num_sms.argtypes = [vp]
             L.gemm_num_pairs.argtypes = [vp]
             L.gemm_row_softmax.argtypes = [vp, i64, i64, vp, vp, vp]
+            L.gemm_attention_fwd.argtypes = [vp, i64, i64, i64, i64, vp, vp, vp, vp, ctypes.c_float, i32, vp]
             L.gemm_set_timeout_ns.argtypes = [vp, ctypes.c_uint64]
             L.gemm_set_debug.argtypes = [vp, i32]
             L.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, i32, vp]
@@ -222,6 +223,33 @@ def row_softmax(ctx, X, out=None, stream=None):
     if stream is None:
         stream = torch.cuda.current_stream(X.device)
     gemm_row_softmax(ctx, rows, cols, X, out, stream)
+    return out
+
+
+def gemm_attention_fwd(ctx, heads, seq_q, seq_k, head_dim, Q, K, V, O, scale, causal, stream=None) -> int:
+    rc = lib().gemm_attention_fwd(_h(ctx), heads, seq_q, seq_k, head_dim, _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+                                  float(scale), int(bool(causal)), _stream(stream, _dev(ctx)))
+    return _check(rc, "gemm_attention_fwd")
+
+
+def attention(ctx, Q, K, V, scale=None, causal=False, out=None, stream=None):
+    """FlashAttention forward on torch CUDA FP16 tensors [heads, seq, 128] through
+    ``gemm_attention_fwd`` (``scale`` defaults to 1/sqrt(128))."""
+    import math
+
+    import torch
+
+    H, Sq, D = Q.shape
+    Sk = K.shape[1]
+    if out is None:
+        out = torch.empty_like(Q)
+    for t in (Q, K, V, out):
+        if t.dtype != torch.float16 or not t.is_contiguous():
+            raise ValueError("Q, K, V and out must be contiguous float16 tensors")
+    if stream is None:
+        stream = torch.cuda.current_stream(Q.device)
+    gemm_attention_fwd(ctx, H, Sq, Sk, D, Q, K, V, out, 1.0 / math.sqrt(D) if scale is None else scale, causal,
+                       stream)
     return out
 
 

@@ -13,6 +13,7 @@
 #include "gemm_kernel.cuh"
 #include "gemm_kernel_pair.cuh"
 #include "softmax_kernel.cuh"
+#include "attention_kernel.cuh"
 
 namespace {
 
@@ -282,6 +283,12 @@ int gemm_create(gemm_ctx **out, int device)
         delete ctx;
         return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);
     }
+    e = cudaFuncSetAttribute(gb300::attention_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gb300::AttnConfig::SMEM_BYTES);
+    if (e != cudaSuccess) {
+        delete ctx;
+        return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);
+    }
     // The pair kernel is used only if the device can co-schedule its clusters.
     if (cudaFuncSetAttribute(gb300::gemm_tcgen05_pair_kernel<PairCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              PairCfg::SMEM_BYTES) == cudaSuccess) {
@@ -518,6 +525,70 @@ const char *gemm_status_string(int status)
 int gemm_num_sms(gemm_ctx *ctx) { return ctx ? ctx->num_sms : 0; }
 
 int gemm_num_pairs(gemm_ctx *ctx) { return ctx ? ctx->max_clusters : 0; }
+
+int gemm_attention_fwd(gemm_ctx *ctx, int64_t heads, int64_t seq_q, int64_t seq_k, int64_t head_dim, const void *Q,
+                       const void *K, const void *V, void *O, float scale, int causal, void *stream)
+{
+    using Cfg = gb300::AttnConfig;
+    if (!ctx || heads < 0 || seq_q < 0 || seq_k < 0 || heads > INT32_MAX || seq_q > INT32_MAX || seq_k > INT32_MAX)
+        return GEMM_ERR_ARG;
+    if (head_dim != Cfg::D || (causal != 0 && causal != 1) || !(scale == scale))
+        return GEMM_ERR_ARG;
+    if (heads == 0 || seq_q == 0)
+        return GEMM_OK;
+    if (seq_k == 0 || !Q || !K || !V || !O)
+        return GEMM_ERR_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+        return GEMM_ERR_ALIGN;
+    const size_t qb = static_cast<size_t>(heads) * seq_q * Cfg::D * 2, kb = static_cast<size_t>(heads) * seq_k * Cfg::D * 2;
+    if (overlaps(O, qb, Q, qb) || overlaps(O, qb, K, kb) || overlaps(O, qb, V, kb))
+        return GEMM_ERR_ARG;
+    const int64_t q_blocks = (seq_q + Cfg::BQ - 1) / Cfg::BQ;
+    if (heads * q_blocks > INT32_MAX)
+        return GEMM_ERR_ARG;
+    if (!on_device(Q, ctx->device) || !on_device(K, ctx->device) || !on_device(V, ctx->device) ||
+        !on_device(O, ctx->device))
+        return GEMM_ERR_DEVICE;
+    DeviceGuard guard(ctx->device);
+    // [head][row][dim] views, 64 x 128 boxes (64 dims = one 128-byte swizzle row, 128 rows)
+    auto encode_3d = [&](CUtensorMap *map, const void *ptr, int64_t rows) {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(Cfg::D), static_cast<cuuint64_t>(rows),
+                                    static_cast<cuuint64_t>(heads)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Cfg::D) * 2, static_cast<cuuint64_t>(rows) * Cfg::D * 2};
+        const cuuint32_t box[3] = {64, 128, 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        return ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    CUtensorMap tq, tk, tv;
+    if (!encode_3d(&tq, Q, seq_q) || !encode_3d(&tk, K, seq_k) || !encode_3d(&tv, V, seq_k))
+        return GEMM_ERR_LAUNCH;
+    gb300::AttnParams p;
+    p.H = static_cast<int>(heads);
+    p.Sq = static_cast<int>(seq_q);
+    p.Sk = static_cast<int>(seq_k);
+    p.q_blocks = static_cast<int>(q_blocks);
+    p.causal = causal;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.O = static_cast<__half *>(O);
+    p.err = ctx->d_err;
+    p.timeout_ns = ctx->timeout_ns;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(heads * q_blocks), 1, 1);
+    cfg.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, gb300::attention_fwd_kernel, tq, tk, tv, p);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+}
+
 
 int gemm_row_softmax(gemm_ctx *ctx, int64_t rows, int64_t cols, const void *X, void *Y, void *stream)
 {
