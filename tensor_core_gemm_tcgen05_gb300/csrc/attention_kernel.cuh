@@ -31,6 +31,20 @@
 
 namespace gb300 {
 
+// 2^x with the MUFU.EX2 instruction (flushes denormal results to zero, which only affects
+// probabilities below 2^-126, far under FP16's smallest value).
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// A row's running maximum is raised (and its row of O rescaled) only when a block's maximum
+// exceeds it by more than this many base-2 units; otherwise probabilities are taken against
+// the old maximum and stay below 2^8, well inside FP16 and FP32.
+constexpr float kRescaleThreshold = 8.0f;
+
 struct AttnParams {
     int H;              // heads (batch x heads)
     int Sq, Sk;         // query and key lengths
@@ -90,11 +104,32 @@ __device__ __forceinline__ uint64_t v_step_desc(uint32_t tile, int kk)
     return sw128_desc(tile + static_cast<uint32_t>(kk) * 2048u, AttnConfig::ATOM_BYTES, 1024);
 }
 
+// Reads the four 32-column chunks of a 128-column TMEM row range starting at `addr` and
+// hands each to fn(chunk registers, chunk index); the load of chunk c+1 is in flight while
+// chunk c is processed. Warp-collective.
+template <class Fn>
+__device__ __forceinline__ void two_buffered_chunks(uint32_t addr, uint32_t (&va)[32], uint32_t (&vb)[32], Fn &&fn)
+{
+    tmem_ld_32x32b_x32(addr, va);
+    tmem_ld_wait_regs(va);
+    tmem_ld_32x32b_x32(addr + 32u, vb);
+    fn(va, 0);
+    tmem_ld_wait_regs(vb);
+    tmem_ld_32x32b_x32(addr + 64u, va);
+    fn(vb, 1);
+    tmem_ld_wait_regs(va);
+    tmem_ld_32x32b_x32(addr + 96u, vb);
+    fn(va, 2);
+    tmem_ld_wait_regs(vb);
+    fn(vb, 3);
+}
+
 // Online softmax of one epilogue warp (warps 2..5): each thread owns query row r of the
 // block (TMEM lane r). Per key block j: (1) read the 128 scores of the row and take their
 // maximum (base-2 units; keys past the sequence, or after the query when causal, are left
 // out); (2) once the previous P V product has finished, rescale the row of O in TMEM by
-// 2^(m_old - m_new) if the maximum grew (skipped when no row of the warp changed); (3) read
+// 2^(m_old - m_new) if the maximum grew by more than kRescaleThreshold (skipped when no row
+// of the warp needs it); (3) read
 // the scores again and write p = 2^(s - m_new) as FP16 into the P tile, K-major with the
 // 128-byte swizzle (16-byte piece c of row r at atom (c / 8), r * 128 + ((c % 8) ^ (r % 8)) * 16),
 // summing p into the running denominator l. At the end the row of O is divided by l.
@@ -111,7 +146,7 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
     const uint32_t o_addr = tmem + lane_base + Cfg::O_COL;
     const int kmax = p.causal ? min(p.Sk - 1, qi) : p.Sk - 1;   // last key this row sees
     float m = -INFINITY, l = 0.0f;
-    uint32_t v[32];
+    uint32_t v[32], va[32], vb[32];
     for (int j = 0; j < n_kv; ++j) {
         const int b = j & 1;
         int w = 1;
@@ -123,19 +158,19 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
         const uint32_t s_addr = tmem + lane_base + Cfg::S_COL + static_cast<uint32_t>(b) * 128u;
         const int k0 = j * Cfg::BKV;
         float mb = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            tmem_ld_32x32b_x32(s_addr + 32u * c, v);
-            tmem_ld_wait_regs(v);
+        auto max_chunk = [&](const uint32_t(&x)[32], int c) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const float x = __uint_as_float(v[e]) * p.scale_log2;
-                mb = (k0 + 32 * c + e <= kmax) ? fmaxf(mb, x) : mb;
+                const float t = __uint_as_float(x[e]) * p.scale_log2;
+                mb = (k0 + 32 * c + e <= kmax) ? fmaxf(mb, t) : mb;
             }
-        }
-        const float m_new = fmaxf(m, mb);
+        };
+        two_buffered_chunks(s_addr, va, vb, max_chunk);
+        // keep the old maximum unless this block's exceeds it by more than the threshold
+        const bool raise = mb > m + kRescaleThreshold || m == -INFINITY;
+        const float m_new = raise ? mb : m;
         const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-        const float alpha = exp2f(m - m_use);   // 0 on the first block (m = -inf)
+        const float alpha = raise ? fast_exp2(m - m_use) : 1.0f;   // 0 on the first block (m = -inf)
         if (j > 0) {
             if (lane == 0)
                 w = wait_bounded(pv_done, static_cast<uint32_t>(j - 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
@@ -156,10 +191,7 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
             }
         }
         float sum = 0.0f;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            tmem_ld_32x32b_x32(s_addr + 32u * c, v);
-            tmem_ld_wait_regs(v);
+        auto p_chunk = [&](const uint32_t(&x)[32], int c) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 uint32_t pk[4];
@@ -167,8 +199,9 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
                 for (int e = 0; e < 4; ++e) {
                     const int idx = 8 * i + 2 * e;
                     const int k = k0 + 32 * c + idx;
-                    const float p0 = k <= kmax ? exp2f(__uint_as_float(v[idx]) * p.scale_log2 - m_use) : 0.0f;
-                    const float p1 = k + 1 <= kmax ? exp2f(__uint_as_float(v[idx + 1]) * p.scale_log2 - m_use) : 0.0f;
+                    const float p0 = k <= kmax ? fast_exp2(fmaf(__uint_as_float(x[idx]), p.scale_log2, -m_use)) : 0.0f;
+                    const float p1 =
+                        k + 1 <= kmax ? fast_exp2(fmaf(__uint_as_float(x[idx + 1]), p.scale_log2, -m_use)) : 0.0f;
                     sum += p0 + p1;
                     __half2 hh = __floats2half2_rn(p0, p1);
                     pk[e] = *reinterpret_cast<uint32_t *>(&hh);
@@ -179,7 +212,8 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
                                       ((static_cast<uint32_t>(kc & 7) ^ static_cast<uint32_t>(r & 7)) << 4);
                 st_shared_v4(addr, make_uint4(pk[0], pk[1], pk[2], pk[3]));
             }
-        }
+        };
+        two_buffered_chunks(s_addr, va, vb, p_chunk);
         l = l * alpha + sum;
         m = m_new;
         fence_proxy_async_shared();   // P is read by the tensor cores (async proxy)
