@@ -176,33 +176,46 @@ __device__ __forceinline__ bool wait_until(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
-#ifndef GB300_GELU_AS7126
-#define GB300_GELU_AS7126 0
-#endif
-
-#if GB300_GELU_AS7126
-// GELU(x) = x * Phi(x), Phi(x) = 1 - erfc(x / sqrt(2)) / 2 for x >= 0 and erfc(|x| / sqrt(2)) / 2
-// for x < 0. erfc(z), z >= 0, from Abramowitz & Stegun, Handbook of Mathematical Functions,
-// formula 7.1.26 (Hastings): erfc(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
-// t = 1 / (1 + p z), absolute error <= 1.5e-7. Branch-free; no cancellation for x < 0.
-__device__ __forceinline__ float gelu_erf(float x)
+// GELU of two accumulator values at once: GELU(x) = x * Phi(x), with the normal CDF
+// Phi(x) = 1 - h for x >= 0 and h for x < 0, where h = erfc(|x| / sqrt(2)) / 2.
+// erfc(z), z >= 0, from Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26 (Hastings): erfc(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2) with
+// t = 1 / (1 + p z), absolute error at most 1.5e-7 (the 1/2 of h is folded into a1..a5).
+// Both signs in one expression: with g = x h (0 <= h <= 1/2), GELU(x) = max(x - g, g), since
+// g <= x / 2 <= x - g when x >= 0 and x - g = x (1 - h) <= x h = g when x < 0.
+// Cost: the reciprocal and the exponential run on the special-function unit; everything else
+// is six packed f32x2 instructions per pair plus two max. Extra FP32 instructions in the
+// epilogue warps slow the concurrent MMAs of the next tile, so the count matters: this form
+// costs about a third of a scalar erff-based one.
+__device__ __forceinline__ void gelu_pair(float &x0, float &x1)
 {
-    const float z = fabsf(x) * 0.70710678118654752f;
-    const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
-    float poly = fmaf(t, 1.061405429f, -1.453152027f);
-    poly = fmaf(t, poly, 1.421413741f);
-    poly = fmaf(t, poly, -0.284496736f);
-    poly = fmaf(t, poly, 0.254829592f);
-    const float erfc_z = poly * t * __expf(-z * z);
-    const float phi = x >= 0.0f ? fmaf(-0.5f, erfc_z, 1.0f) : 0.5f * erfc_z;
-    return x * phi;
+    constexpr double kL2e = 1.4426950408889634;
+    constexpr double kInvSqrt2 = 0.70710678118654752;
+    const uint64_t x = f32x2_pack(x0, x1);
+    const uint64_t ax = x & 0x7FFFFFFF7FFFFFFFull;   // |x0|, |x1|
+    const uint64_t d = f32x2_fma(ax, f32x2_pack(static_cast<float>(0.3275911 * kInvSqrt2),
+                                                static_cast<float>(0.3275911 * kInvSqrt2)),
+                                 f32x2_pack(1.0f, 1.0f));
+    float d0, d1;
+    f32x2_unpack(d, d0, d1);
+    const uint64_t t = f32x2_pack(rcp_approx(d0), rcp_approx(d1));
+    auto splat = [](double c) { return f32x2_pack(static_cast<float>(c), static_cast<float>(c)); };
+    uint64_t q = f32x2_fma(splat(0.5 * 1.061405429), t, splat(0.5 * -1.453152027));
+    q = f32x2_fma(q, t, splat(0.5 * 1.421413741));
+    q = f32x2_fma(q, t, splat(0.5 * -0.284496736));
+    q = f32x2_fma(q, t, splat(0.5 * 0.254829592));
+    // exp(-z^2) = 2^(-x^2 log2(e) / 2)
+    const uint64_t e_arg = f32x2_mul(f32x2_mul(x, splat(-0.5 * kL2e)), x);
+    float a0, a1;
+    f32x2_unpack(e_arg, a0, a1);
+    const uint64_t h = f32x2_mul(t, f32x2_mul(q, f32x2_pack(ex2_approx(a0), ex2_approx(a1))));
+    const uint64_t g = f32x2_mul(x, h);
+    float g0, g1, r0, r1;
+    f32x2_unpack(g, g0, g1);
+    f32x2_unpack(f32x2_sub(x, g), r0, r1);
+    x0 = fmaxf(r0, g0);
+    x1 = fmaxf(r1, g1);
 }
-#else
-__device__ __forceinline__ float gelu_erf(float x)
-{
-    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
-}
-#endif
 
 // Same as tcgen05.wait::ld, and ties the 32 destination registers of the load it waits
 // for to this point, so that no use of them can be scheduled before the wait.
@@ -250,15 +263,16 @@ __device__ __forceinline__ void epilogue_math_stage(const GemmParams &p, const u
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 f = __half22float2(bh[e]);
-                v[8 * i + 2 * e] += f.x;
-                v[8 * i + 2 * e + 1] += f.y;
+                const uint64_t sum = f32x2_add(f32x2_pack(v[8 * i + 2 * e], v[8 * i + 2 * e + 1]),
+                                               f32x2_pack(f.x, f.y));
+                f32x2_unpack(sum, v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
             }
         }
     }
     if (p.epilogue == EPI_GELU) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            v[j] = gelu_erf(v[j]);
+        for (int j = 0; j < 32; j += 2)
+            gelu_pair(v[j], v[j + 1]);
     } else if (p.epilogue == EPI_RELU) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
