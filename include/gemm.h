@@ -20,7 +20,10 @@
  * one round-to-nearest-even conversion to FP16, one store.
  *
  * Threading: a context may be used by one host thread at a time (or with external
- * serialisation). Calls on different contexts are independent.
+ * serialisation). Calls on different contexts are independent. GEMMs of one context that
+ * take the stream-K schedule (see gemm_run) share the context's workspace, so they must not
+ * run at the same time on the GPU: keep one context's GEMMs on one stream (or in stream
+ * order), or give each concurrently used stream a context of its own.
  */
 #ifndef GB300_GEMM_H
 #define GB300_GEMM_H
@@ -32,7 +35,9 @@ extern "C" {
 #endif
 
 /* Opaque context: cached device properties, the tensor-map encoder, a 4-byte device
- * error word and (only once gemm_run_host has been called) host-path staging buffers. */
+ * error word, the stream-K workspace (128 KB of FP32 partial sums and a few ready flags
+ * per SM, about 19.5 MB on GB300) and (only once gemm_run_host has been called) host-path
+ * staging buffers. */
 typedef struct gemm_ctx gemm_ctx;
 
 /* Epilogue selector. The bias is applied whenever `bias` is non-NULL, for every value. */
@@ -67,7 +72,8 @@ enum gemm_status {
 
 /* Create a context for CUDA device `device` (0-based). Checks that the device has compute
  * capability 10.3 (GB300, sm_103a), reads its SM count, sets the kernel's shared-memory
- * attribute, resolves cuTensorMapEncodeTiled and allocates the 4-byte device error word.
+ * attribute, resolves cuTensorMapEncodeTiled and allocates the 4-byte device error word and
+ * the stream-K workspace.
  * On success *out receives the context (caller frees it with gemm_destroy) and GEMM_OK is
  * returned; on failure *out is set to NULL. The caller's current device is left as it was. */
 int gemm_create(gemm_ctx **out, int device);
@@ -87,6 +93,13 @@ int gemm_create(gemm_ctx **out, int device);
  *   epilogue: a gemm_epilogue value.
  * Ownership: the caller owns every buffer and must keep them alive until the stream has
  * passed this call. gemm_run allocates nothing and launches exactly one kernel.
+ * Schedule: 256 x 256 tiles on CTA pairs when there are at least as many as co-resident
+ * pairs; otherwise 128 x 256 tiles on single SMs, and when those are at most half the SMs
+ * and K gives at least twice as many CTAs as tiles 16 k-blocks of 64 each, stream-K: the
+ * tiles' k-blocks are split evenly over up to every SM, and a tile cut between SMs is
+ * summed in FP32 through the context's workspace before its epilogue (so the summation
+ * order, not the result's tolerance, differs from the whole-tile schedule). Never for
+ * GEMM_EPI_SOFTMAX.
  * Errors: see gemm_status. A wait that runs out inside the kernel is reported later by
  * gemm_last_device_error, not by this call. */
 int gemm_run(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, const void *B,
@@ -109,15 +122,18 @@ int gemm_run_host(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A,
 /* After the caller has synchronised the stream(s) that ran this context's GEMMs: return
  * GEMM_OK, or GEMM_ERR_TIMEOUT if a bounded in-kernel wait ran out since the last call.
  * `detail` (may be NULL) receives the raw error word (which wait ran out: 1 producer
- * slot, 2 MMA operands, 3 MMA accumulator, 4 epilogue accumulator, 5 teardown drain).
- * Clears the word. Synchronous (a 4-byte device-to-host copy). */
+ * slot, 2 MMA operands, 3 MMA accumulator, 4 epilogue accumulator, 5 teardown drain,
+ * 6 stream-K partial sum from another SM). Clears the word, and after an error also the
+ * stream-K ready flags a kernel that gave up may have left raised (call it before the next
+ * GEMM on this context once a timeout is possible). Synchronous. */
 int gemm_last_device_error(gemm_ctx *ctx, uint32_t *detail);
 
 /* The last CUDA runtime error code seen by this context (0 if none), for diagnosis of
  * GEMM_ERR_LAUNCH / GEMM_ERR_NOMEM. */
 int gemm_last_cuda_error(gemm_ctx *ctx);
 
-/* Destroy a context (NULL is accepted). Frees the error word and any staging buffers; the
+/* Destroy a context (NULL is accepted). Frees the error word, the stream-K workspace and
+ * any staging buffers; the
  * caller must have synchronised every stream that still runs work of this context. */
 int gemm_destroy(gemm_ctx *ctx);
 
@@ -173,12 +189,16 @@ int gemm_attention_fwd(gemm_ctx *ctx, int64_t heads, int64_t seq_q, int64_t seq_
  *       the kernel must take its timeout path (a flag that nothing sets; no fault, no hang);
  *     GEMM_DEBUG_FORCE_SINGLE / GEMM_DEBUG_FORCE_PAIR: override the kernel choice, so that
  *       tests can run any shape through either kernel (FORCE_PAIR is ignored when the
- *       pair kernel cannot run). */
+ *       pair kernel cannot run);
+ *     GEMM_DEBUG_FORCE_STREAMK: the one-CTA kernel always takes the stream-K schedule,
+ *       with one CTA per k-block unit up to one per SM (so that tiles are cut into many
+ *       parts), except for GEMM_EPI_SOFTMAX. */
 enum {
     GEMM_DEBUG_NONE = 0,
     GEMM_DEBUG_WITHHOLD_FIRST_LOAD = 1,
     GEMM_DEBUG_FORCE_SINGLE = 2,
-    GEMM_DEBUG_FORCE_PAIR = 4
+    GEMM_DEBUG_FORCE_PAIR = 4,
+    GEMM_DEBUG_FORCE_STREAMK = 8
 };
 int gemm_set_timeout_ns(gemm_ctx *ctx, uint64_t ns);
 int gemm_set_debug(gemm_ctx *ctx, int flags);

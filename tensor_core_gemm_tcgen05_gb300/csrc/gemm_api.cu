@@ -47,6 +47,14 @@ constexpr int kSoftmaxMaxN = 256;   // one tile spans the whole output row
 constexpr int kHostChunksMax = 8;
 constexpr size_t kHostChunkMinBytes = size_t(32) << 20;
 constexpr uint64_t kMinTimeoutNs = 1000000ull;
+// Stream-K (one-CTA kernel): each CTA gets at least this many (tile, k-block) units, and
+// stream-K is taken only when it runs at least twice as many CTAs as there are tiles. The
+// hand-off of a cut tile (partials written, pulled in by the owner, added in TMEM) costs a
+// few microseconds on the critical path; measured on GB300, it pays off for 32 tiles of
+// 128 x 256 x 8192 (39.8 -> 28.0 us) but not for 128 tiles on 152 SMs (2048^3: 15.3 us
+// whole tiles, 23 us stream-K).
+constexpr int64_t kStreamKMinUnits = 16;
+constexpr int kStreamKMinSpread = 2;
 
 }  // namespace
 
@@ -59,6 +67,10 @@ struct gemm_ctx {
     int debug = 0;
     int last_cuda_error = 0;
     int max_clusters = 0;   // co-resident CTA pairs of the pair kernel (0: pair kernel unusable)
+    // stream-K workspace: one FP32 128 x 256 partial accumulator per SM, and per SM one
+    // ready flag per epilogue warp (zero between launches)
+    float *sk_ws = nullptr;
+    uint32_t *sk_flags = nullptr;
     // gemm_run_host: device staging buffers, two copy streams and the events that order
     // the chunked pipeline (created on first use)
     void *stage = nullptr;
@@ -238,8 +250,25 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
         p.n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
         p.num_tiles = p.m_blocks * p.n_blocks;
         p.group_m = raster_group(p.m_blocks, Cfg::BM, K);
-        const int grid = std::min(p.num_tiles, ctx->num_sms);
-        launch_pdl(gb300::gemm_tcgen05_kernel<Cfg>, grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
+        int grid = std::min(p.num_tiles, ctx->num_sms);
+        // Stream-K when the tiles leave most SMs idle: the (tile, k-block) units are split
+        // evenly over up to every SM (the fused softmax needs whole rows in one CTA: never).
+        const int64_t units = static_cast<int64_t>(p.num_tiles) * p.num_kb;
+        if (epilogue != GEMM_EPI_SOFTMAX && units > 0) {
+            int g_sk = 0;
+            if (ctx->debug & GEMM_DEBUG_FORCE_STREAMK)
+                g_sk = static_cast<int>(std::min<int64_t>(ctx->num_sms, units));
+            else if (static_cast<int64_t>(p.num_tiles) * kStreamKMinSpread <= ctx->num_sms)
+                g_sk = static_cast<int>(std::min<int64_t>(ctx->num_sms, units / kStreamKMinUnits));
+            if (g_sk >= kStreamKMinSpread * p.num_tiles || ((ctx->debug & GEMM_DEBUG_FORCE_STREAMK) && g_sk > 0)) {
+                p.sk_units = units;
+                p.sk_ws = ctx->sk_ws;
+                p.sk_flags = ctx->sk_flags;
+                grid = g_sk;
+            }
+        }
+        launch_pdl(p.sk_units > 0 ? gb300::gemm_tcgen05_kernel<Cfg, true> : gb300::gemm_tcgen05_kernel<Cfg, false>, grid,
+                   Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -277,8 +306,11 @@ int gemm_create(gemm_ctx **out, int device)
     ctx->device = device;
     ctx->num_sms = sms;
     DeviceGuard guard(device);
-    cudaError_t e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg>,
+    cudaError_t e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_BYTES);
     if (e != cudaSuccess) {
         delete ctx;
         return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);
@@ -309,12 +341,24 @@ int gemm_create(gemm_ctx **out, int device)
         return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);
     }
     ctx->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    const size_t ws_bytes = static_cast<size_t>(sms) * Cfg::BM * Cfg::BN * sizeof(float);
+    const size_t flag_bytes = static_cast<size_t>(sms) * Cfg::NUM_EPI_WARPS * sizeof(uint32_t);
     e = cudaMalloc(&ctx->d_err, sizeof(uint32_t));
     if (e == cudaSuccess)
         e = cudaMemset(ctx->d_err, 0, sizeof(uint32_t));
+    if (e == cudaSuccess)
+        e = cudaMalloc(&ctx->sk_ws, ws_bytes);
+    if (e == cudaSuccess)
+        e = cudaMalloc(&ctx->sk_flags, flag_bytes);
+    if (e == cudaSuccess)
+        e = cudaMemset(ctx->sk_flags, 0, flag_bytes);
     if (e != cudaSuccess) {
         if (ctx->d_err)
             cudaFree(ctx->d_err);
+        if (ctx->sk_ws)
+            cudaFree(ctx->sk_ws);
+        if (ctx->sk_flags)
+            cudaFree(ctx->sk_flags);
         delete ctx;
         return cuda_fail(nullptr, e, GEMM_ERR_NOMEM);
     }
@@ -469,6 +513,9 @@ int gemm_last_device_error(gemm_ctx *ctx, uint32_t *detail)
     cudaError_t e = cudaMemcpy(&w, ctx->d_err, sizeof(w), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && w != 0)
         e = cudaMemset(ctx->d_err, 0, sizeof(uint32_t));
+    // a kernel that gave up may have left stream-K ready flags raised: lower them all
+    if (e == cudaSuccess && w != 0)
+        e = cudaMemset(ctx->sk_flags, 0, static_cast<size_t>(ctx->num_sms) * Cfg::NUM_EPI_WARPS * sizeof(uint32_t));
     if (e != cudaSuccess)
         return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
     if (detail)
@@ -486,6 +533,10 @@ int gemm_destroy(gemm_ctx *ctx)
         DeviceGuard guard(ctx->device);
         if (ctx->d_err)
             cudaFree(ctx->d_err);
+        if (ctx->sk_ws)
+            cudaFree(ctx->sk_ws);
+        if (ctx->sk_flags)
+            cudaFree(ctx->sk_flags);
         if (ctx->stage)
             cudaFree(ctx->stage);
         for (int i = 0; i < kHostChunksMax; ++i) {
@@ -632,7 +683,8 @@ int gemm_set_timeout_ns(gemm_ctx *ctx, uint64_t ns)
 
 int gemm_set_debug(gemm_ctx *ctx, int flags)
 {
-    if (!ctx || (flags & ~(GEMM_DEBUG_WITHHOLD_FIRST_LOAD | GEMM_DEBUG_FORCE_SINGLE | GEMM_DEBUG_FORCE_PAIR)))
+    if (!ctx || (flags & ~(GEMM_DEBUG_WITHHOLD_FIRST_LOAD | GEMM_DEBUG_FORCE_SINGLE | GEMM_DEBUG_FORCE_PAIR |
+                           GEMM_DEBUG_FORCE_STREAMK)))
         return GEMM_ERR_ARG;
     ctx->debug = flags;
     return GEMM_OK;

@@ -22,6 +22,15 @@
 //    rows with tcgen05.ld, adds the bias, applies the activation in FP32, rounds to FP16
 //    and writes 16-byte vectors, masking rows >= M and columns >= N.
 //    While it drains accumulator b, the MMA warp already fills accumulator b ^ 1.
+//  * stream-K (when there are fewer tiles than SMs): the tile-major sequence of
+//    (tile, 64-wide k-block) units is cut into one equal range per CTA, so every SM gets the
+//    same share of the MMAs however many tiles there are. A tile cut by range boundaries is
+//    summed by the CTA holding its first k-block (its "owner", which reaches that part last
+//    in its range): every other CTA with a part of the tile (reached first in its range)
+//    writes its FP32 partial accumulator to a workspace slot of its own and raises a ready
+//    flag; the owner waits for the flags, pulls each partial into its (by then idle) operand
+//    ring with one bulk copy per warp, adds it to the accumulator in Tensor Memory, runs the
+//    epilogue and lowers the flags again for the next launch.
 //
 // Every mbarrier wait is bounded in time. When a wait runs out the kernel records which
 // one in a device error word, tells the other roles to stop, waits (bounded) for its own
@@ -44,6 +53,7 @@ enum : uint32_t {
     ERR_MMA_ACCUMULATOR = 3,
     ERR_EPILOGUE_ACCUMULATOR = 4,
     ERR_TEARDOWN_DRAIN = 5,
+    ERR_STREAMK_PARTIAL = 6,   // a stream-K owner waited too long for another CTA's partial
 };
 
 enum : int { EPI_NONE = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_SOFTMAX = 3 };
@@ -64,6 +74,11 @@ struct GemmParams {
     uint32_t *err;         // device error word
     uint64_t timeout_ns;   // limit of every wait
     int debug;             // DEBUG_* flags
+    // stream-K (one-CTA kernel): 0 = whole tiles per CTA; else the number of
+    // (tile, k-block) units, split into gridDim.x equal ranges
+    int64_t sk_units = 0;
+    float *sk_ws = nullptr;          // [gridDim.x][epilogue warp][chunk][8][32 lanes][4] FP32 partials
+    uint32_t *sk_flags = nullptr;    // [gridDim.x][epilogue warps]: 1 = that part is written
 };
 
 template <int BM_, int BN_, int STAGES_, int EPI_WARPS_ = 4>
@@ -84,7 +99,12 @@ struct KernelConfig {
     static constexpr int NUM_EPI_WARPS = EPI_WARPS_;
     static constexpr int EPI_COL_GROUPS = NUM_EPI_WARPS / 4;   // warps sharing a TMEM quarter
     static constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+    // full[s], empty[s], acc_full[b], acc_empty[b], drain, one stream-K partial barrier per
+    // epilogue warp
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + NUM_EPI_WARPS;
+    // stream-K: one epilogue warp's share of a partial accumulator (32 rows x its columns,
+    // FP32), as stored in the workspace and as pulled into the operand ring
+    static constexpr int PART_WARP_BYTES = (BN / EPI_COL_GROUPS) * 32 * 4;
     // after the ring: barriers, TMEM address, stop flag; then one BN-wide bias slice per
     // epilogue warp (FP16)
     static constexpr int BIAS_OFFSET = STAGES * STAGE_BYTES + ((NUM_BARS * 8 + 16 + 15) / 16) * 16;
@@ -98,6 +118,7 @@ struct KernelConfig {
     static_assert(NUM_EPI_WARPS == 4 || NUM_EPI_WARPS == 8, "one or two warps per TMEM lane quarter");
     static_assert((BN / 32) % EPI_COL_GROUPS == 0, "column chunks split evenly between warps");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+    static_assert(NUM_EPI_WARPS * PART_WARP_BYTES <= STAGES * STAGE_BYTES, "partials fit the operand ring");
 };
 
 // UMMA shared-memory descriptor for a 128-byte-swizzled operand tile.
@@ -135,6 +156,50 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int t, int &mb,
     mb = first_m + r % rows;
     nb = r / rows;
 }
+
+// First stream-K unit of CTA g (the range of CTA g ends where that of g + 1 begins).
+__device__ __forceinline__ int64_t sk_begin(const GemmParams &p, int g)
+{
+    return static_cast<int64_t>(g) * p.sk_units / static_cast<int64_t>(gridDim.x);
+}
+
+// The work of this CTA as segments: k-blocks [k0, k1) of one tile. Whole tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ... (k0 = 0, k1 = num_kb), or, with stream-K, the pieces of the
+// tiles that the CTA's unit range covers, in order.
+template <bool STREAM_K>
+struct WorkIter {
+    int64_t u = 0, end = 0;
+    int t = 0;
+    __device__ explicit WorkIter(const GemmParams &p)
+    {
+        if constexpr (STREAM_K) {
+            u = sk_begin(p, static_cast<int>(blockIdx.x));
+            end = sk_begin(p, static_cast<int>(blockIdx.x) + 1);
+        } else {
+            t = static_cast<int>(blockIdx.x);
+        }
+    }
+    __device__ bool next(const GemmParams &p, int &tile, int &k0, int &k1)
+    {
+        if constexpr (STREAM_K) {
+            if (u >= end)
+                return false;
+            tile = static_cast<int>(u / p.num_kb);
+            k0 = static_cast<int>(u - static_cast<int64_t>(tile) * p.num_kb);
+            k1 = static_cast<int>(min(static_cast<int64_t>(p.num_kb), k0 + (end - u)));
+            u += k1 - k0;
+            return true;
+        } else {
+            if (t >= p.num_tiles)
+                return false;
+            tile = t;
+            k0 = 0;
+            k1 = p.num_kb;
+            t += static_cast<int>(gridDim.x);
+            return true;
+        }
+    }
+};
 
 struct WaitCtl {
     volatile int *abort;   // shared-memory stop flag
@@ -393,6 +458,103 @@ __device__ __forceinline__ void epilogue_softmax_tile(const GemmParams &p, uint3
     }
 }
 
+// Stream-K: a CTA holding a later part of a tile writes its warp's share of the FP32
+// accumulator (32 rows, up to CHUNKS chunks of 32 columns starting at TMEM `taddr` /
+// output column `n_first`) to its workspace slot. Layout of the warp's share (at `dst`):
+// chunk c, then 16-byte piece i (columns 4i..4i+3 of the chunk), then the lane (row), so
+// that each store instruction of the warp writes 512 contiguous bytes and the owner can
+// fetch the whole share with one bulk copy. Chunks past N and rows past M are skipped, as
+// the owner skips them.
+template <int CHUNKS>
+__device__ __forceinline__ void epilogue_partial_store(const GemmParams &p, uint32_t taddr, float *dst, int n_first,
+                                                       int row0, int lane)
+{
+    const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
+    if (valid <= 0 || row0 >= p.M)
+        return;
+    uint32_t ra[32], rb[32];
+    auto put = [&](const uint32_t(&r)[32], int c) {
+        float4 *d = reinterpret_cast<float4 *>(dst) + c * 256 + lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            __stcg(d + 32 * i, make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                           __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+    };
+    tmem_ld_32x32b_x32(taddr, ra);
+#pragma unroll 1
+    for (int c = 0; c < valid; c += 2) {
+        tmem_ld_wait_regs(ra);
+        if (c + 1 < valid)
+            tmem_ld_32x32b_x32(taddr + 32u * (c + 1), rb);
+        put(ra, c);
+        if (c + 1 < valid) {
+            tmem_ld_wait_regs(rb);
+            if (c + 2 < valid)
+                tmem_ld_32x32b_x32(taddr + 32u * (c + 2), ra);
+            put(rb, c + 1);
+        }
+    }
+}
+
+// Stream-K owner: add one contributor's share (already in shared memory at `buf`, laid out
+// as epilogue_partial_store wrote it) to this warp's rows of the accumulator in TMEM.
+template <int CHUNKS>
+__device__ __forceinline__ void fold_partial(uint32_t taddr, uint32_t buf, int valid, int lane)
+{
+#pragma unroll 1
+    for (int c = 0; c < valid; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + 32u * c, r);
+        float4 q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)   // consecutive lanes read consecutive 16-byte pieces
+            q[i] = ld_shared_f4(buf + static_cast<uint32_t>((c * 256 + 32 * i + lane) * 16));
+        tmem_ld_wait_regs(r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint64_t lo = f32x2_add(f32x2_pack(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])),
+                                          f32x2_pack(q[i].x, q[i].y));
+            const uint64_t hi = f32x2_add(f32x2_pack(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])),
+                                          f32x2_pack(q[i].z, q[i].w));
+            float a, b, d, e;
+            f32x2_unpack(lo, a, b);
+            f32x2_unpack(hi, d, e);
+            r[4 * i] = __float_as_uint(a);
+            r[4 * i + 1] = __float_as_uint(b);
+            r[4 * i + 2] = __float_as_uint(d);
+            r[4 * i + 3] = __float_as_uint(e);
+        }
+        tmem_st_32x32b_x32(taddr + 32u * c, r);
+    }
+    tmem_st_wait();
+}
+
+// Stream-K owner: wait (all lanes of the warp together) until `flag` is 1, bounded like every
+// other wait; false if the limit ran out or another role of this CTA gave up.
+__device__ __forceinline__ bool wait_flag(const uint32_t *flag, const WaitCtl &w, int lane)
+{
+    if (__all_sync(0xffffffffu, ld_acquire_gpu_u32(flag) == 1u))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(64);
+        if (__all_sync(0xffffffffu, ld_acquire_gpu_u32(flag) == 1u))
+            return true;
+        int stop = 0;
+        if (lane == 0) {
+            if (*w.abort) {
+                stop = 1;
+            } else if (global_timer_ns() - t0 > w.limit_ns) {
+                *w.abort = 1;
+                atomicCAS(w.err, 0u, static_cast<uint32_t>(ERR_STREAMK_PARTIAL));
+                stop = 1;
+            }
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0))
+            return false;
+    }
+}
+
 // Epilogue of one warp for one tile, step 2 (accumulator ready): up to CHUNKS chunks of 32
 // columns starting at TMEM address `taddr` / output column `n_first`, for the 32 output rows
 // starting at `row0`. The TMEM load of chunk c+1 is in flight while chunk c is processed;
@@ -453,7 +615,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t tadd
     }
 }
 
-template <class Cfg>
+// STREAM_K: the stream-K schedule (p.sk_units > 0, workspace and flags set); otherwise whole
+// tiles per CTA (p.sk_* unused).
+template <class Cfg, bool STREAM_K = false>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
@@ -469,10 +633,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const uint32_t sB = base + STAGES * Cfg::A_BYTES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sp + STAGES * Cfg::STAGE_BYTES);
     const uint32_t bar0 = smem_u32(bars);
-    // barrier k lives at bar0 + 8k: full[s], empty[s], acc_full[b], acc_empty[b], drain
+    // barrier k lives at bar0 + 8k: full[s], empty[s], acc_full[b], acc_empty[b], drain,
+    // part[epilogue warp]
     const uint32_t full0 = bar0, empty0 = bar0 + 8u * STAGES;
     const uint32_t accf0 = bar0 + 16u * STAGES, acce0 = accf0 + 8u * Cfg::ACC_BUFS;
-    const uint32_t drain = acce0 + 8u * Cfg::ACC_BUFS;
+    const uint32_t drain = acce0 + 8u * Cfg::ACC_BUFS, part0 = drain + 8u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     uint4 *bias_stage = reinterpret_cast<uint4 *>(sp + Cfg::BIAS_OFFSET);
@@ -491,6 +656,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             mbar_init(acce0 + 8u * b, Cfg::NUM_EPI_WARPS);
         }
         mbar_init(drain, 1);
+        for (int w = 0; w < Cfg::NUM_EPI_WARPS; ++w)
+            mbar_init(part0 + 8u * w, 1);
         *abort_flag = 0;
         fence_mbar_init();
         if (p.num_kb > 0) {
@@ -519,10 +686,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_parity = 0;
             bool ok = true, withhold = (p.debug & DEBUG_WITHHOLD_FIRST_LOAD) != 0;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            WorkIter<STREAM_K> work(p);
+            int t, k0, k1;
+            while (ok && work.next(p, t, k0, k1)) {
                 int mb, nb;
                 tile_coords(p, t, mb, nb);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = k0; kb < k1; ++kb) {
                     if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, wc, ERR_PRODUCER_SLOT)) {
                         ok = false;
                         break;
@@ -559,14 +728,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            WorkIter<STREAM_K> work(p);
+            int t, k0, k1;
+            while (ok && work.next(p, t, k0, k1)) {
                 if (!wait_bounded(acce0 + 8u * acc, acc_phase ^ 1u, wc, ERR_MMA_ACCUMULATOR)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = k0; kb < k1; ++kb) {
                     if (!wait_bounded(full0 + 8u * stage, phase, wc, ERR_MMA_OPERANDS)) {
                         ok = false;
                         break;
@@ -582,7 +753,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         // B, MN-major: 16 K-rows are 2048 bytes further; 8-row K groups are
                         // 1024 bytes apart (SBO); 64-column N atoms are one box apart (LBO).
                         const uint64_t bdesc = sw128_desc(b0 + kk * 2048, Cfg::B_BOX_BYTES, 1024);
-                        umma_f16<1>(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        umma_f16<1>(d_tmem, adesc, bdesc, IDESC, (kb != k0 || kk != 0) ? 1u : 0u);
                     }
                     umma_commit(empty0 + 8u * stage);   // slot free once these MMAs have read it
                     if (++stage == STAGES) {
@@ -615,7 +786,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         uint32_t box_sel = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        const int ew = warp - 2;   // this warp's stream-K flag and partial-barrier index
+        // floats per workspace slot, and the offset of this warp's share in a slot
+        constexpr int64_t SLOT = static_cast<int64_t>(BM) * BN;
+        const int64_t my_share = static_cast<int64_t>(ew) * (Cfg::PART_WARP_BYTES / 4);
+        uint32_t part_phase = 0;
+        WorkIter<STREAM_K> work(p);
+        int t, k0, k1;
+        while (work.next(p, t, k0, k1)) {
             int mb, nb;
             tile_coords(p, t, mb, nb);
             const uint4 bv = bias_fetch(p, nb * BN, lane);
@@ -626,14 +804,60 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             if (!ok)
                 break;
             tc_fence_after_sync();
-            if (p.bias != nullptr) {
-                my_bias[lane] = bv;
+            const uint32_t tacc = tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c_begin * 32);
+            const int n_first = nb * BN + c_begin * 32, row0 = mb * BM + quarter * 32;
+            if (STREAM_K && k0 > 0) {
+                // a later part of a cut tile: hand the partial sum to the tile's owner
+                epilogue_partial_store<CHUNKS>(p, tacc, p.sk_ws + static_cast<int64_t>(blockIdx.x) * SLOT + my_share,
+                                               n_first, row0, lane);
+                __threadfence();
                 __syncwarp();
+                if (lane == 0)
+                    st_release_gpu_u32(p.sk_flags + blockIdx.x * Cfg::NUM_EPI_WARPS + ew, 1u);
+            } else {
+                int n_parts = 0;
+                if (STREAM_K && k1 < p.num_kb) {
+                    // Owner of a cut tile: the CTAs whose ranges begin inside it hold the rest.
+                    // This is the last part of this CTA's range, so its MMAs are complete and
+                    // the operand ring is idle: each warp pulls a contributor's share into its
+                    // own piece of the ring and adds it to its rows in TMEM.
+                    const int64_t tile_end = static_cast<int64_t>(t + 1) * p.num_kb;
+                    const int g0 = static_cast<int>(blockIdx.x);
+                    while (g0 + n_parts + 1 < static_cast<int>(gridDim.x) && sk_begin(p, g0 + n_parts + 1) < tile_end)
+                        ++n_parts;
+                    const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
+                    const bool inside = valid > 0 && row0 < p.M;
+                    const uint32_t buf = sA + static_cast<uint32_t>(ew * Cfg::PART_WARP_BYTES);
+                    for (int j = 1; ok && j <= n_parts; ++j) {
+                        ok = wait_flag(p.sk_flags + (g0 + j) * Cfg::NUM_EPI_WARPS + ew, wc, lane) ? 1 : 0;
+                        if (!ok || !inside)
+                            continue;
+                        if (lane == 0) {
+                            fence_proxy_async_global();   // acquired data, read next by the copy engine
+                            mbar_arrive_expect_tx(part0 + 8u * ew, Cfg::PART_WARP_BYTES);
+                            bulk_load_g2s(buf, p.sk_ws + static_cast<int64_t>(g0 + j) * SLOT + my_share,
+                                          Cfg::PART_WARP_BYTES, part0 + 8u * ew);
+                            ok = wait_bounded(part0 + 8u * ew, part_phase, wc, ERR_STREAMK_PARTIAL) ? 1 : 0;
+                        }
+                        part_phase ^= 1u;
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (ok)
+                            fold_partial<CHUNKS>(tacc, buf, valid, lane);
+                    }
+                    if (!ok)
+                        break;
+                }
+                if (p.bias != nullptr) {
+                    my_bias[lane] = bv;
+                    __syncwarp();
+                }
+                epilogue_tile<CHUNKS>(p, tacc, n_first, row0, p.bias != nullptr ? my_bias + c_begin * 4 : nullptr,
+                                      &tmap_c, my_stage, box_sel, lane);
+                if (n_parts > 0 && lane == 0) {   // consumed: lower the flags for the next launch
+                    for (int j = 1; j <= n_parts; ++j)
+                        p.sk_flags[(static_cast<int>(blockIdx.x) + j) * Cfg::NUM_EPI_WARPS + ew] = 0u;
+                }
             }
-            epilogue_tile<CHUNKS>(p, tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c_begin * 32),
-                                  nb * BN + c_begin * 32, mb * BM + quarter * 32,
-                                  p.bias != nullptr ? my_bias + c_begin * 4 : nullptr, &tmap_c, my_stage, box_sel,
-                                  lane);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)

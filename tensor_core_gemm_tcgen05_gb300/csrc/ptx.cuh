@@ -201,10 +201,34 @@ __device__ __forceinline__ void fence_proxy_async_shared()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy accesses to global memory with its later async-proxy
+// (TMA / bulk copy) accesses, and the reverse.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Untiled bulk copy global -> this CTA's shared memory, `bytes` (a multiple of 16, both
+// addresses 16-byte aligned), completing on mbarrier `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 // ---- tcgen05: Tensor Memory ----------------------------------------------------------------
@@ -324,6 +348,22 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask
         " [%0], %1;" ::"r"(bar),
         "h"(cta_mask)
         : "memory");
+}
+
+// ---------------------------------------------------------------- flags between CTAs
+// Release store / acquire load of a 32-bit flag in global memory at GPU scope: everything
+// the storing thread wrote before the store is visible to a thread whose acquire load
+// returns the stored value.
+__device__ __forceinline__ void st_release_gpu_u32(uint32_t *addr, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t *addr)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
 }
 
 // ---------------------------------------------------------------- packed FP32 arithmetic

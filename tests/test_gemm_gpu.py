@@ -29,13 +29,22 @@ def ctx():
     c.close()
 
 
-@pytest.fixture(params=["single", "pair"])
+FORCE = {
+    "single": g.GEMM_DEBUG_FORCE_SINGLE,
+    "pair": g.GEMM_DEBUG_FORCE_PAIR,
+    "streamk": g.GEMM_DEBUG_FORCE_SINGLE | g.GEMM_DEBUG_FORCE_STREAMK,
+}
+
+
+@pytest.fixture(params=list(FORCE))
 def kctx(ctx, request):
-    """The context with the kernel choice forced: one-CTA 128x256 tiles or CTA-pair
-    256x256 tiles (cta_group::2)."""
+    """The context with the kernel choice forced: one-CTA 128x256 tiles, CTA-pair 256x256
+    tiles (cta_group::2), or one-CTA tiles under stream-K with one k-block unit per CTA (up
+    to one CTA per SM), so that most tiles are cut into several parts summed through the
+    workspace."""
     if request.param == "pair" and g.gemm_num_pairs(ctx) == 0:
         pytest.skip("the pair kernel cannot run on this device")
-    g.gemm_set_debug(ctx, g.GEMM_DEBUG_FORCE_SINGLE if request.param == "single" else g.GEMM_DEBUG_FORCE_PAIR)
+    g.gemm_set_debug(ctx, FORCE[request.param])
     yield ctx
     g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
 
@@ -307,6 +316,78 @@ def test_bounded_wait_reports_timeout_and_context_survives(ctx, force):
         g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
         g.gemm_set_timeout_ns(ctx, 2_000_000_000)
     check(ctx, 256, 512, 256, epi=g.EPI_GELU, with_bias=True, seed=3)
+
+
+def test_streamk_timeout_then_recovery(ctx):
+    """Stream-K with tiles cut into 16 parts: CTA 0 (owner of tile 0) withholds its first
+    load and gives up, so the ready flags of its 15 contributors stay raised. The timeout
+    is reported, gemm_last_device_error lowers the flags, and the next stream-K GEMM (with
+    different inputs, so stale partials would show) is correct."""
+    g.gemm_set_timeout_ns(ctx, 20_000_000)
+    g.gemm_set_debug(ctx, g.GEMM_DEBUG_WITHHOLD_FIRST_LOAD | FORCE["streamk"])
+    try:
+        dev = torch.device("cuda:0")
+        A = torch.ones(256, 1024, dtype=torch.float16, device=dev)
+        B = torch.ones(1024, 256, dtype=torch.float16, device=dev)
+        C = torch.zeros(256, 256, dtype=torch.float16, device=dev)
+        g.gemm(ctx, A, B, None, g.EPI_NONE, out=C)
+        torch.cuda.synchronize()
+        status, detail = g.gemm_last_device_error(ctx)
+        assert status == g.GEMM_ERR_TIMEOUT and detail in (1, 2, 3, 4, 5, 6)
+        assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+        g.gemm_set_debug(ctx, FORCE["streamk"])
+        check(ctx, 256, 256, 1024, epi=g.EPI_GELU, with_bias=True, seed=12)
+    finally:
+        g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
+        g.gemm_set_timeout_ns(ctx, 2_000_000_000)
+
+
+def test_streamk_graph_replays_with_new_inputs(ctx):
+    """A captured stream-K GEMM replayed with new inputs each time: every owner must wait for
+    this replay's partials (the flags are lowered after use, not left from the last run)."""
+    dev = torch.device("cuda:0")
+    M, N, K = 384, 512, 2048
+    g.gemm_set_debug(ctx, FORCE["streamk"])
+    try:
+        dA = torch.empty(M, K, dtype=torch.float16, device=dev)
+        dB = inputs.random_fp16((K, N), 91).to(dev)
+        C = torch.empty(M, N, dtype=torch.float16, device=dev)
+        g.gemm(ctx, dA.zero_(), dB, None, g.EPI_NONE, out=C)   # first call outside capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            g.gemm(ctx, dA, dB, None, g.EPI_NONE, out=C)
+        for seed in (92, 93, 94):
+            A = inputs.random_fp16((M, K), seed)
+            dA.copy_(A.to(dev))
+            graph.replay()
+            torch.cuda.synchronize()
+            assert_parity(C.cpu().numpy(), oracle_ref(A, dB.cpu(), None, g.EPI_NONE), f"replay {seed}")
+        assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+    finally:
+        g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
+
+
+def test_default_streamk_on_few_tiles(ctx):
+    """1024 x 1024 x 8192 + bias + GELU on the default schedule: 32 tiles of 128 x 256 on
+    ~150 SMs take stream-K (each tile cut into ~5 parts). Against the oracle on sampled
+    rows, and bit-identical between two runs (the parts are added in a fixed order)."""
+    M, N, K = 1024, 1024, 8192
+    A = inputs.random_fp16((M, K), 61, "normal")
+    B = inputs.random_fp16((K, N), 62, "normal_inv_k", k=K)
+    bias = inputs.random_fp16((N,), 63)
+    dev = torch.device("cuda:0")
+    C1 = torch.empty(M, N, dtype=torch.float16, device=dev)
+    C2 = torch.empty(M, N, dtype=torch.float16, device=dev)
+    dA, dB, db = A.to(dev), B.to(dev), bias.to(dev)
+    g.gemm(ctx, dA, dB, db, g.EPI_GELU, out=C1)
+    g.gemm(ctx, dA, dB, db, g.EPI_GELU, out=C2)
+    torch.cuda.synchronize()
+    assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+    assert torch.equal(C1, C2)
+    rows = inputs.sample_rows(M, 96, seed=5, include_last=2).numpy()
+    rows = np.union1d(rows, [0, 127, 128, 511, 512, 1023])
+    assert_parity(C1.cpu().numpy()[rows], oracle_ref(A, B, bias, g.EPI_GELU, rows=rows), "stream-K default")
 
 
 def test_host_buffer_entry_point(ctx):
