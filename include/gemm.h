@@ -46,9 +46,13 @@ enum gemm_epilogue {
     GEMM_EPI_GELU = 1, /* C = GELU_erf(A*B (+ bias))                                 */
     GEMM_EPI_RELU = 2, /* C = max(A*B (+ bias), 0)                                   */
     GEMM_EPI_SOFTMAX = 3 /* C[r][:] = softmax over the row of A*B (+ bias): the logits stay
-                            in FP32 inside the kernel and are never written. Needs
-                            N <= 256 (one tile spans the whole row); larger N returns
-                            GEMM_ERR_ARG (run GEMM_EPI_NONE, then gemm_row_softmax).
+                            in FP32 inside the kernel and are never written. N <= 256:
+                            one tile spans the row. 256 < N <= 4096: a thread-block
+                            cluster of ceil(N/256) CTAs spans it and merges per-CTA row
+                            maxima and sums through distributed shared memory (cluster
+                            sizes above 8 need the device to schedule them; a width it
+                            cannot schedule, or N > 4096, returns GEMM_ERR_ARG: run
+                            GEMM_EPI_NONE, then gemm_row_softmax).
                             "Designing High-Performance GPU Kernels with TileLang"
                             (spaxe.top): row-wise softmax in the GEMM epilogue.       */
 };
@@ -123,7 +127,8 @@ int gemm_run_host(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A,
  * GEMM_OK, or GEMM_ERR_TIMEOUT if a bounded in-kernel wait ran out since the last call.
  * `detail` (may be NULL) receives the raw error word (which wait ran out: 1 producer
  * slot, 2 MMA operands, 3 MMA accumulator, 4 epilogue accumulator, 5 teardown drain,
- * 6 stream-K partial sum from another SM). Clears the word, and after an error also the
+ * 6 stream-K partial sum from another SM, 7 row statistics from the other CTAs of a
+ * softmax row cluster). Clears the word, and after an error also the
  * stream-K ready flags a kernel that gave up may have left raised (call it before the next
  * GEMM on this context once a timeout is possible). Synchronous. */
 int gemm_last_device_error(gemm_ctx *ctx, uint32_t *detail);

@@ -25,6 +25,9 @@ using Cfg = gb300::KernelConfig<128, 256, 4, GB300_EPI_WARPS>;
 #define GB300_PAIR_STAGES 6
 #endif
 using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS>;
+// The softmax epilogue's kernel: the same 128 x 256 tiles, a shorter ring (softmax GEMMs have
+// small K) and eight epilogue warps, two per TMEM lane quarter, each with half of the columns.
+using SmCfg = gb300::KernelConfig<128, 256, 3, 8>;
 #ifndef GB300_GROUP_PANEL_MB
 #define GB300_GROUP_PANEL_MB 32
 #endif
@@ -41,7 +44,8 @@ int raster_group(int m_blocks, int rows_per_block, int K)
     return static_cast<int>(std::max<int64_t>(kMinGroup, std::min<int64_t>(m_blocks, g)));
 }
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
-constexpr int kSoftmaxMaxN = 256;   // one tile spans the whole output row
+constexpr int kSoftmaxTileN = 256;    // columns of C per CTA of a softmax row cluster
+constexpr int kRowClusterMax = 16;    // clusters of up to 16 CTAs (N <= 4096)
 // gemm_run_host splits M into at most this many chunks whose uploads, GEMMs and downloads
 // overlap; outputs smaller than kHostChunkMinBytes are not split.
 constexpr int kHostChunksMax = 8;
@@ -71,6 +75,9 @@ struct gemm_ctx {
     // ready flag per epilogue warp (zero between launches)
     float *sk_ws = nullptr;
     uint32_t *sk_flags = nullptr;
+    // softmax epilogue: co-resident clusters of cs CTAs (one per 256 columns), per cs
+    // (0: that cluster size cannot be scheduled)
+    int row_clusters[kRowClusterMax + 1] = {};
     // gemm_run_host: device staging buffers, two copy streams and the events that order
     // the chunked pipeline (created on first use)
     void *stage = nullptr;
@@ -150,8 +157,12 @@ int check_args(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, co
         return GEMM_OK;
     if (!C || (K > 0 && (!A || !B)))
         return GEMM_ERR_ARG;
-    if (epilogue == GEMM_EPI_SOFTMAX && (N > kSoftmaxMaxN || Cfg::EPI_COL_GROUPS != 1))
-        return GEMM_ERR_ARG;   // the fused softmax needs whole rows inside one tile and one warp
+    if (epilogue == GEMM_EPI_SOFTMAX) {
+        // a row takes a cluster of ceil(N / 256) CTAs
+        const int64_t cs = (N + kSoftmaxTileN - 1) / kSoftmaxTileN;
+        if (cs > kRowClusterMax || ctx->row_clusters[cs] == 0)
+            return GEMM_ERR_ARG;
+    }
     if (N % 8 != 0 || K % 8 != 0)
         return GEMM_ERR_ALIGN;
     if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B))) || (bias && !aligned16(bias)))
@@ -200,6 +211,28 @@ void launch_pdl(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, gb300::Gem
     cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p);
 }
 
+// The same with a cluster of `cluster` CTAs along x (grid a multiple of it).
+void launch_pdl_cluster(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, gb300::GemmParams), int grid,
+                        int cluster, int threads, int smem, cudaStream_t stream, const CUtensorMap &ta,
+                        const CUtensorMap &tb, const CUtensorMap &tc, const gb300::GemmParams &p)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p);
+}
+
 // ldb / ldc: row strides of B and C in elements (0: N, tightly packed); A is always packed.
 // gemm_run_host uses them to run column bands of a larger B and C.
 int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, const void *bias, void *C,
@@ -231,6 +264,22 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     p.debug = ctx->debug & GEMM_DEBUG_WITHHOLD_FIRST_LOAD;
     // 256 x 256 tiles on CTA pairs when there are enough of them to give every pair at
     // least one; otherwise 128 x 256 tiles on single SMs (twice as many tiles to spread).
+    if (epilogue == GEMM_EPI_SOFTMAX) {
+        // one cluster of n_blocks CTAs (a single CTA when N <= 256) per 128-row block
+        static_assert(SmCfg::BM == Cfg::BM && SmCfg::BN == Cfg::BN && SmCfg::BK == Cfg::BK &&
+                          SmCfg::B_BOX_N == Cfg::B_BOX_N,
+                      "same tensor-map boxes as the GEMM kernel");
+        p.m_blocks = (M + SmCfg::BM - 1) / SmCfg::BM;
+        p.n_blocks = (N + SmCfg::BN - 1) / SmCfg::BN;
+        p.num_tiles = p.m_blocks * p.n_blocks;
+        p.group_m = 1;
+        p.row_cluster = p.n_blocks;
+        const int clusters = std::min(p.m_blocks, ctx->row_clusters[p.n_blocks]);
+        launch_pdl_cluster(gb300::gemm_tcgen05_kernel<SmCfg, gb300::SCHED_ROW_CLUSTER>, clusters * p.n_blocks,
+                           p.n_blocks, SmCfg::NUM_THREADS, SmCfg::SMEM_BYTES, stream, ta, tb, tc, p);
+        const cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? GEMM_OK : cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+    }
     const int pair_tiles = ((M + PairCfg::BM - 1) / PairCfg::BM) * ((N + PairCfg::BN - 1) / PairCfg::BN);
     bool pair = ctx->max_clusters > 0 && pair_tiles >= ctx->max_clusters;
     if (ctx->debug & GEMM_DEBUG_FORCE_SINGLE)
@@ -267,8 +316,9 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
                 grid = g_sk;
             }
         }
-        launch_pdl(p.sk_units > 0 ? gb300::gemm_tcgen05_kernel<Cfg, true> : gb300::gemm_tcgen05_kernel<Cfg, false>, grid,
-                   Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
+        launch_pdl(p.sk_units > 0 ? gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_STREAM_K>
+                                  : gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_TILES>,
+                   grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -306,11 +356,11 @@ int gemm_create(gemm_ctx **out, int device)
     ctx->device = device;
     ctx->num_sms = sms;
     DeviceGuard guard(device);
-    cudaError_t e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg, false>,
+    cudaError_t e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_TILES>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg::SMEM_BYTES);
+        e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_STREAM_K>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) {
         delete ctx;
         return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);
@@ -333,6 +383,32 @@ int gemm_create(gemm_ctx **out, int device)
             ctx->max_clusters = clusters;
     }
     cudaGetLastError();
+    // Softmax row clusters: how many clusters of each size fit at once (sizes above 8 need
+    // the non-portable cluster attribute; a size that cannot be scheduled stays 0 and the
+    // widths it would serve are refused).
+    {
+        auto *rk = gb300::gemm_tcgen05_kernel<SmCfg, gb300::SCHED_ROW_CLUSTER>;
+        if (cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize, SmCfg::SMEM_BYTES) == cudaSuccess &&
+            cudaFuncSetAttribute(rk, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+            for (int cs = 1; cs <= kRowClusterMax; ++cs) {
+                cudaLaunchConfig_t lc = {};
+                lc.gridDim = dim3(static_cast<unsigned>(cs * (sms / cs)), 1, 1);
+                lc.blockDim = dim3(SmCfg::NUM_THREADS, 1, 1);
+                lc.dynamicSmemBytes = SmCfg::SMEM_BYTES;
+                cudaLaunchAttribute a[1];
+                a[0].id = cudaLaunchAttributeClusterDimension;
+                a[0].val.clusterDim.x = static_cast<unsigned>(cs);
+                a[0].val.clusterDim.y = 1;
+                a[0].val.clusterDim.z = 1;
+                lc.attrs = a;
+                lc.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, rk, &lc) == cudaSuccess)
+                    ctx->row_clusters[cs] = n;
+            }
+        }
+        cudaGetLastError();
+    }
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);

@@ -31,6 +31,13 @@
 //    flag; the owner waits for the flags, pulls each partial into its (by then idle) operand
 //    ring with one bulk copy per warp, adds it to the accumulator in Tensor Memory, runs the
 //    epilogue and lowers the flags again for the next launch.
+//  * row clusters (the softmax epilogue over rows wider than one tile, 256 < N <= 4096): a
+//    thread-block cluster of ceil(N / 256) CTAs owns a 128-row block, CTA r computing column
+//    tile r. Each epilogue thread reduces its row over its CTA's columns (running maximum and
+//    sum of exponentials), the CTAs exchange these per-row statistics through distributed
+//    shared memory (mbarrier arrivals on every CTA of the cluster, then ld.shared::cluster),
+//    and each CTA normalises its own tile from Tensor Memory: the logits never leave the
+//    chip and C is written once.
 //
 // Every mbarrier wait is bounded in time. When a wait runs out the kernel records which
 // one in a device error word, tells the other roles to stop, waits (bounded) for its own
@@ -54,6 +61,14 @@ enum : uint32_t {
     ERR_EPILOGUE_ACCUMULATOR = 4,
     ERR_TEARDOWN_DRAIN = 5,
     ERR_STREAMK_PARTIAL = 6,   // a stream-K owner waited too long for another CTA's partial
+    ERR_ROW_EXCHANGE = 7,      // a row cluster waited too long for the other CTAs' row statistics
+};
+
+// How a launch maps work to CTAs (the kernel's SCHED template argument).
+enum : int {
+    SCHED_TILES = 0,         // whole tiles, grouped raster, persistent
+    SCHED_STREAM_K = 1,      // equal ranges of (tile, k-block) units
+    SCHED_ROW_CLUSTER = 2,   // one cluster per 128-row block, CTA r = column tile r
 };
 
 enum : int { EPI_NONE = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_SOFTMAX = 3 };
@@ -79,6 +94,7 @@ struct GemmParams {
     int64_t sk_units = 0;
     float *sk_ws = nullptr;          // [gridDim.x][epilogue warp][chunk][8][32 lanes][4] FP32 partials
     uint32_t *sk_flags = nullptr;    // [gridDim.x][epilogue warps]: 1 = that part is written
+    int row_cluster = 0;             // row clusters: CTAs per cluster (= n_blocks)
 };
 
 template <int BM_, int BN_, int STAGES_, int EPI_WARPS_ = 4>
@@ -100,8 +116,8 @@ struct KernelConfig {
     static constexpr int EPI_COL_GROUPS = NUM_EPI_WARPS / 4;   // warps sharing a TMEM quarter
     static constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
     // full[s], empty[s], acc_full[b], acc_empty[b], drain, one stream-K partial barrier per
-    // epilogue warp
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + NUM_EPI_WARPS;
+    // epilogue warp, row-cluster stats_ready[2] and stats_read[2]
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + NUM_EPI_WARPS + 4;
     // stream-K: one epilogue warp's share of a partial accumulator (32 rows x its columns,
     // FP32), as stored in the workspace and as pulled into the operand ring
     static constexpr int PART_WARP_BYTES = (BN / EPI_COL_GROUPS) * 32 * 4;
@@ -110,7 +126,12 @@ struct KernelConfig {
     static constexpr int BIAS_OFFSET = STAGES * STAGE_BYTES + ((NUM_BARS * 8 + 16 + 15) / 16) * 16;
     // then, 1024-aligned, two 32 x 32 FP16 output staging boxes per epilogue warp
     static constexpr int STORE_OFFSET = ((BIAS_OFFSET + NUM_EPI_WARPS * BN * 2 + 1023) / 1024) * 1024;
-    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES;
+    // then the softmax row statistics: the cluster exchange's two buffers of (max, sum) per
+    // row, and (two column groups) the groups' two buffers of (max, sum) per row and group
+    static constexpr int STATS_OFFSET = STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES;
+    static constexpr int PAIR_OFFSET = STATS_OFFSET + 2 * BM * 8;
+    static constexpr int SMEM_BYTES =
+        1024 /* alignment slack */ + PAIR_OFFSET + (EPI_COL_GROUPS == 2 ? 2 * BM * 2 * 8 : 0);
 
     static_assert(BM == 128, "one CTA, M = 128: TMEM lane i holds tile row i");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
@@ -163,39 +184,58 @@ __device__ __forceinline__ int64_t sk_begin(const GemmParams &p, int g)
     return static_cast<int64_t>(g) * p.sk_units / static_cast<int64_t>(gridDim.x);
 }
 
-// The work of this CTA as segments: k-blocks [k0, k1) of one tile. Whole tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ... (k0 = 0, k1 = num_kb), or, with stream-K, the pieces of the
-// tiles that the CTA's unit range covers, in order.
-template <bool STREAM_K>
+// The work of this CTA as segments: k-blocks [k0, k1) of output tile t = (mb, nb).
+//  SCHED_TILES: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ... in the grouped raster.
+//  SCHED_STREAM_K: the pieces of the tiles that the CTA's unit range covers, in order.
+//  SCHED_ROW_CLUSTER: row blocks clusterid, clusterid + clusters, ...; column tile = the
+//  CTA's rank in its cluster.
+template <int SCHED>
 struct WorkIter {
     int64_t u = 0, end = 0;
-    int t = 0;
+    int t = 0, step = 0, rank = 0;
     __device__ explicit WorkIter(const GemmParams &p)
     {
-        if constexpr (STREAM_K) {
+        if constexpr (SCHED == SCHED_STREAM_K) {
             u = sk_begin(p, static_cast<int>(blockIdx.x));
             end = sk_begin(p, static_cast<int>(blockIdx.x) + 1);
+        } else if constexpr (SCHED == SCHED_ROW_CLUSTER) {
+            t = static_cast<int>(cluster_id_x());
+            step = static_cast<int>(cluster_count_x());
+            rank = static_cast<int>(cluster_ctarank());
         } else {
             t = static_cast<int>(blockIdx.x);
+            step = static_cast<int>(gridDim.x);
         }
     }
-    __device__ bool next(const GemmParams &p, int &tile, int &k0, int &k1)
+    __device__ bool next(const GemmParams &p, int &tile, int &mb, int &nb, int &k0, int &k1)
     {
-        if constexpr (STREAM_K) {
+        if constexpr (SCHED == SCHED_STREAM_K) {
             if (u >= end)
                 return false;
             tile = static_cast<int>(u / p.num_kb);
             k0 = static_cast<int>(u - static_cast<int64_t>(tile) * p.num_kb);
             k1 = static_cast<int>(min(static_cast<int64_t>(p.num_kb), k0 + (end - u)));
             u += k1 - k0;
+            tile_coords(p, tile, mb, nb);
+            return true;
+        } else if constexpr (SCHED == SCHED_ROW_CLUSTER) {
+            if (t >= p.m_blocks)
+                return false;
+            mb = t;
+            nb = rank;
+            tile = mb * p.n_blocks + nb;
+            k0 = 0;
+            k1 = p.num_kb;
+            t += step;
             return true;
         } else {
             if (t >= p.num_tiles)
                 return false;
             tile = t;
+            tile_coords(p, tile, mb, nb);
             k0 = 0;
             k1 = p.num_kb;
-            t += static_cast<int>(gridDim.x);
+            t += step;
             return true;
         }
     }
@@ -360,24 +400,143 @@ __device__ __forceinline__ void epilogue_math_stage(const GemmParams &p, const u
     }
 }
 
+// Row softmax epilogue: what one epilogue warp needs to merge its rows' statistics with those
+// of the other warps covering the same rows (the other column group of its CTA, and the CTAs
+// of a row cluster) for one tile.
+struct RowExchange {
+    uint32_t stats;    // cluster exchange: [2 buffers][128 rows] x (max, sum) of this CTA
+    uint32_t pair;     // column groups: [2 buffers][128 rows][2 groups] x (max, sum)
+    uint32_t ready0;   // stats_ready[2]: one warp per lane quarter of every CTA has published
+    uint32_t read0;    // stats_read[2]: every epilogue warp of every CTA has read this buffer
+    int cs;            // CTAs in the cluster (1: no cluster exchange)
+    int quarter;       // this warp's TMEM lane quarter
+    int group;         // this warp's column group
+    uint32_t buf;      // buffer of this tile (tile count % 2)
+    uint32_t use;      // earlier uses of that buffer (tile count / 2)
+    const WaitCtl *wc;
+};
+
+// Bounded wait on a local barrier whose phase is completed by arrivals from the cluster.
+__device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity, const WaitCtl &w, uint32_t code)
+{
+    if (mbar_try_wait_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_cluster(bar, parity))
+            return true;
+        if (*w.abort)
+            return false;
+        if (global_timer_ns() - t0 > w.limit_ns) {
+            *w.abort = 1;
+            atomicCAS(w.err, 0u, code);
+            return false;
+        }
+    }
+}
+
+// Merge (m, s) into the running (M, S): M = max, S = sum of s * 2^(m - M) (base-2 units).
+__device__ __forceinline__ void merge_stats(float &M, float &S, float m, float s)
+{
+    if (m == -INFINITY)
+        return;
+    if (m > M) {
+        S = S * ex2_approx(M - m) + s;   // M = -inf gives 2^-inf = 0
+        M = m;
+    } else {
+        S += s * ex2_approx(m - M);
+    }
+}
+
+// Row statistics exchange, step 1: turn this thread's statistics of its row piece (m:
+// maximum in base-2 units, s: sum of 2^(x - m)) into those of the CTA's part of the row and,
+// in a cluster, publish them. With two column groups the pair of warps of a lane quarter
+// merge through shared memory behind a 64-thread named barrier. In a cluster the group-0
+// warp writes the CTA's row statistics and arrives on every CTA's stats_ready barrier (lane r
+// on CTA r: one instruction for all). All 32 lanes call it; false if a wait ran out.
+template <int GROUPS>
+__device__ __forceinline__ bool row_publish(const RowExchange &x, float &m, float &s, int row, int lane)
+{
+    static_assert(GROUPS == 1 || GROUPS == 2, "one or two column groups");
+    if constexpr (GROUPS == 2) {
+        const uint32_t slot = x.pair + ((x.buf * 128u + static_cast<uint32_t>(row)) * 2u) * 8u;
+        st_shared_f2(slot + static_cast<uint32_t>(x.group) * 8u, m, s);
+        named_barrier_sync(1u + static_cast<uint32_t>(x.quarter), 64u);
+        const float2 o = ld_shared_f2(slot + static_cast<uint32_t>(x.group ^ 1) * 8u);
+        merge_stats(m, s, o.x, o.y);
+    }
+    if (x.cs == 1 || x.group != 0)
+        return true;
+    int ok = 1;
+    if (x.use > 0 && lane == 0)   // everyone has read what this buffer held last time
+        ok = wait_cluster_bounded(x.read0 + 8u * x.buf, (x.use - 1u) & 1u, *x.wc, ERR_ROW_EXCHANGE) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, ok, 0))
+        return false;
+    st_shared_f2(x.stats + (x.buf * 128u + static_cast<uint32_t>(row)) * 8u, m, s);
+    __syncwarp();
+    if (lane < x.cs)   // release: the statistics above
+        mbar_arrive_cluster(mapa_shared(x.ready0 + 8u * x.buf, static_cast<uint32_t>(lane)));
+    return true;
+}
+
+// Step 2 (clusters only): wait until every CTA has published, read every CTA's entry for
+// this row through distributed shared memory (all reads issued before the merge), merge
+// them into the whole row's (m, s) and arrive on every CTA's stats_read barrier. All 32
+// lanes call it; false if a wait ran out.
+__device__ __forceinline__ bool row_collect(const RowExchange &x, float &m, float &s, int row, int lane)
+{
+    if (x.cs == 1)
+        return true;
+    int ok = 1;
+    if (lane == 0)
+        ok = wait_cluster_bounded(x.ready0 + 8u * x.buf, x.use & 1u, *x.wc, ERR_ROW_EXCHANGE) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, ok, 0))
+        return false;
+    const uint32_t slot = x.stats + (x.buf * 128u + static_cast<uint32_t>(row)) * 8u;
+    float M = -INFINITY, S = 0.0f;
+#pragma unroll
+    for (int r0 = 0; r0 < 16; r0 += 8) {
+        if (r0 >= x.cs)
+            break;
+        float2 v[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+            if (r0 + r < x.cs)
+                v[r] = ld_shared_cluster_f2(mapa_shared(slot, static_cast<uint32_t>(r0 + r)));
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+            if (r0 + r < x.cs)
+                merge_stats(M, S, v[r].x, v[r].y);
+    }
+    __syncwarp();
+    if (lane < x.cs)   // release: the reads above
+        mbar_arrive_cluster(mapa_shared(x.read0 + 8u * x.buf, static_cast<uint32_t>(lane)));
+    m = M;
+    s = S;
+    return true;
+}
+
 // Row-softmax epilogue ("Designing High-Performance GPU Kernels with TileLang", spaxe.top:
 // softmax applied to each row of the GEMM result in the epilogue, no intermediate written to
-// global memory). Valid when the tile spans every column of C (N <= BN) and one warp owns all
-// columns of its 32 rows: then each thread holds one whole row of logits in its TMEM lane
-// and needs no other thread. Pass 1 reads the row chunk by chunk and keeps a running maximum
-// m and a sum s of exp(x - m) rescaled whenever m grows; pass 2 reads the row again from
-// TMEM and stores exp(x - m) / s (columns at or past N are left out of both passes).
+// global memory). Each thread owns one row (its TMEM lane) and this warp's CHUNKS chunks of
+// 32 columns of it (chunks [0, valid) lie inside C; `active`: the warp's rows start inside C).
+//
+// Pass 1, per chunk: logits (+ bias) in base-2 units, the chunk maximum mc[c], p = 2^(x - mc)
+// written back over the accumulator in TMEM, and the chunk's sum of p, merged into (m, s).
+// One exponential per element; columns at or past N contribute nothing.
 template <int CHUNKS>
-__device__ __forceinline__ void epilogue_softmax_tile(const GemmParams &p, uint32_t taddr, int n_first, int row0,
-                                                      const uint4 *sbias, const CUtensorMap *tmap_c,
-                                                      uint32_t stage, uint32_t &box_sel, int lane)
+__device__ __forceinline__ void softmax_pass1(const GemmParams &p, uint32_t taddr, int n_first, int valid, bool active,
+                                              const uint4 *sbias, float (&mc)[CHUNKS], float &m, float &s)
 {
     constexpr float kL2e = 1.4426950408889634f;
-    const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
-    if (valid <= 0 || row0 >= p.M)
-        return;
     const bool has_acc = p.num_kb > 0;
-    auto logits = [&](int c, float (&v)[32]) {
+    m = -INFINITY;
+    s = 0.0f;
+#pragma unroll
+    for (int c = 0; c < CHUNKS; ++c) {
+        mc[c] = -INFINITY;
+        if (!active || c >= valid)
+            continue;
         uint32_t r[32];
         if (has_acc) {
             tmem_ld_32x32b_x32(taddr + 32u * c, r);
@@ -387,9 +546,7 @@ __device__ __forceinline__ void epilogue_softmax_tile(const GemmParams &p, uint3
             for (int j = 0; j < 32; ++j)
                 r[j] = 0u;
         }
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            v[j] = __uint_as_float(r[j]);
+        float v[32];
         if (sbias != nullptr) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -398,39 +555,63 @@ __device__ __forceinline__ void epilogue_softmax_tile(const GemmParams &p, uint3
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 f = __half22float2(bh[e]);
-                    v[8 * i + 2 * e] += f.x;
-                    v[8 * i + 2 * e + 1] += f.y;
+                    const uint64_t t = f32x2_mul(f32x2_add(f32x2_pack(__uint_as_float(r[8 * i + 2 * e]),
+                                                                      __uint_as_float(r[8 * i + 2 * e + 1])),
+                                                           f32x2_pack(f.x, f.y)),
+                                                 f32x2_pack(kL2e, kL2e));
+                    f32x2_unpack(t, v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
                 }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const uint64_t t = f32x2_mul(f32x2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                             f32x2_pack(kL2e, kL2e));
+                f32x2_unpack(t, v[j], v[j + 1]);
             }
         }
         const int n0 = n_first + 32 * c;
+        if (n0 + 32 > p.N) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (n0 + j >= p.N)
-                v[j] = -INFINITY;   // not a column of C
-    };
-    float m = -INFINITY, s = 0.0f;
-#pragma unroll 1
-    for (int c = 0; c < valid; ++c) {
-        float v[32];
-        logits(c, v);
-        float vm = v[0];
+            for (int j = 0; j < 32; ++j)
+                if (n0 + j >= p.N)
+                    v[j] = -INFINITY;   // not a column of C: contributes 2^-inf = 0
+        }
+        float cm = v[0];
 #pragma unroll
         for (int j = 1; j < 32; ++j)
-            vm = fmaxf(vm, v[j]);
-        const float mn = fmaxf(m, vm);
-        float add = 0.0f;
+            cm = fmaxf(cm, v[j]);
+        float cs = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            add += exp2f((v[j] - mn) * kL2e);
-        s = s * exp2f((m - mn) * kL2e) + add;
-        m = mn;
+        for (int j = 0; j < 32; ++j) {
+            const float e = ex2_approx(v[j] - cm);
+            cs += e;
+            r[j] = __float_as_uint(e);
+        }
+        tmem_st_32x32b_x32(taddr + 32u * c, r);
+        mc[c] = cm;
+        merge_stats(m, s, cm, cs);
     }
+    if (active)
+        tmem_st_wait();
+}
+
+// Pass 2, with the whole row's (m, s): every p of chunk c times 2^(mc[c] - m) / s, to FP16,
+// staged in the warp's 32 x 32 boxes and written by TMA.
+template <int CHUNKS>
+__device__ __forceinline__ void softmax_pass2(uint32_t taddr, int n_first, int row0, int valid,
+                                              const float (&mc)[CHUNKS], float m, float s,
+                                              const CUtensorMap *tmap_c, uint32_t stage, uint32_t &box_sel, int lane)
+{
     const float inv = 1.0f / s;
-#pragma unroll 1
-    for (int c = 0; c < valid; ++c) {
-        float v[32];
-        logits(c, v);
+#pragma unroll
+    for (int c = 0; c < CHUNKS; ++c) {
+        if (c >= valid)
+            break;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + 32u * c, r);
+        const float scale = ex2_approx(mc[c] - m) * inv;
+        tmem_ld_wait_regs(r);
         const uint32_t box = stage + box_sel * EPI_STORE_BOX_BYTES;
         if (lane == 0)
             bulk_wait_group_read<1>();
@@ -442,8 +623,12 @@ __device__ __forceinline__ void epilogue_softmax_tile(const GemmParams &p, uint3
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                __half2 h = __floats2half2_rn(exp2f((v[8 * i + 2 * e] - m) * kL2e) * inv,
-                                              exp2f((v[8 * i + 2 * e + 1] - m) * kL2e) * inv);
+                const uint64_t q = f32x2_mul(f32x2_pack(__uint_as_float(r[8 * i + 2 * e]),
+                                                        __uint_as_float(r[8 * i + 2 * e + 1])),
+                                             f32x2_pack(scale, scale));
+                float a, b;
+                f32x2_unpack(q, a, b);
+                __half2 h = __floats2half2_rn(a, b);
                 w[e] = *reinterpret_cast<uint32_t *>(&h);
             }
             st_shared_v4(row_base + ((static_cast<uint32_t>(i) ^ sw) << 4), make_uint4(w[0], w[1], w[2], w[3]));
@@ -456,6 +641,30 @@ __device__ __forceinline__ void epilogue_softmax_tile(const GemmParams &p, uint3
         }
         box_sel ^= 1u;
     }
+}
+
+// The whole softmax epilogue of one tile: pass 1, the row statistics exchange (with `xch`:
+// several warps or CTAs cover the row), pass 2. Without `xch` the warp must cover every
+// column of C (N <= CHUNKS * 32).
+template <int CHUNKS, int GROUPS>
+__device__ __forceinline__ void epilogue_softmax_tile(const GemmParams &p, uint32_t taddr, int n_first, int row0,
+                                                      const uint4 *sbias, const CUtensorMap *tmap_c,
+                                                      uint32_t stage, uint32_t &box_sel, int lane,
+                                                      const RowExchange *xch)
+{
+    const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
+    const bool active = valid > 0 && row0 < p.M;
+    if (!active && xch == nullptr)
+        return;   // (a warp of an exchange still publishes and reads statistics)
+    float mc[CHUNKS], m, s;
+    softmax_pass1<CHUNKS>(p, taddr, n_first, valid, active, sbias, mc, m, s);
+    if (xch != nullptr) {
+        const int row = static_cast<int>(row0 % 128) + lane;
+        if (!row_publish<GROUPS>(*xch, m, s, row, lane) || !row_collect(*xch, m, s, row, lane))
+            return;
+    }
+    if (active)
+        softmax_pass2<CHUNKS>(taddr, n_first, row0, valid, mc, m, s, tmap_c, stage, box_sel, lane);
 }
 
 // Stream-K: a CTA holding a later part of a tile writes its warp's share of the FP32
@@ -561,13 +770,13 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *flag, const WaitCtl &w
 // each finished 32 x 32 box goes out with one TMA store from the warp's two alternating
 // staging boxes (`stage`, toggled through `box_sel`), which clips rows >= M and
 // columns >= N. Called by all 32 lanes together (tcgen05.ld is warp-collective).
-template <int CHUNKS>
+template <int CHUNKS, int GROUPS = 1>
 __device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t taddr, int n_first, int row0,
                                               const uint4 *sbias, const CUtensorMap *tmap_c, uint32_t stage,
-                                              uint32_t &box_sel, int lane)
+                                              uint32_t &box_sel, int lane, const RowExchange *xch = nullptr)
 {
     if (p.epilogue == EPI_SOFTMAX) {
-        epilogue_softmax_tile<CHUNKS>(p, taddr, n_first, row0, sbias, tmap_c, stage, box_sel, lane);
+        epilogue_softmax_tile<CHUNKS, GROUPS>(p, taddr, n_first, row0, sbias, tmap_c, stage, box_sel, lane, xch);
         return;
     }
     const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
@@ -615,9 +824,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t tadd
     }
 }
 
-// STREAM_K: the stream-K schedule (p.sk_units > 0, workspace and flags set); otherwise whole
-// tiles per CTA (p.sk_* unused).
-template <class Cfg, bool STREAM_K = false>
+// SCHED: SCHED_TILES (whole tiles per CTA), SCHED_STREAM_K (p.sk_units > 0, workspace and
+// flags set) or SCHED_ROW_CLUSTER (launched in clusters of p.row_cluster = n_blocks CTAs,
+// softmax epilogue only).
+template <class Cfg, int SCHED = SCHED_TILES>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
@@ -638,6 +848,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const uint32_t full0 = bar0, empty0 = bar0 + 8u * STAGES;
     const uint32_t accf0 = bar0 + 16u * STAGES, acce0 = accf0 + 8u * Cfg::ACC_BUFS;
     const uint32_t drain = acce0 + 8u * Cfg::ACC_BUFS, part0 = drain + 8u;
+    const uint32_t stats_ready0 = part0 + 8u * Cfg::NUM_EPI_WARPS, stats_read0 = stats_ready0 + 16u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     uint4 *bias_stage = reinterpret_cast<uint4 *>(sp + Cfg::BIAS_OFFSET);
@@ -658,6 +869,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         mbar_init(drain, 1);
         for (int w = 0; w < Cfg::NUM_EPI_WARPS; ++w)
             mbar_init(part0 + 8u * w, 1);
+        // row clusters: one warp per lane quarter of every CTA publishes, every epilogue warp
+        // of every CTA reads, once per phase
+        const uint32_t pub = SCHED == SCHED_ROW_CLUSTER ? static_cast<uint32_t>(p.row_cluster * 4) : 1u;
+        const uint32_t rd = SCHED == SCHED_ROW_CLUSTER ? static_cast<uint32_t>(p.row_cluster * Cfg::NUM_EPI_WARPS) : 1u;
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(stats_ready0 + 8u * b, pub);
+            mbar_init(stats_read0 + 8u * b, rd);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         if (p.num_kb > 0) {
@@ -665,6 +884,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             tma_prefetch_desc(&tmap_b);
         }
         tma_prefetch_desc(&tmap_c);
+    }
+    if constexpr (SCHED == SCHED_ROW_CLUSTER) {
+        __syncwarp();
+        cluster_sync();   // every CTA's barriers exist before any remote arrival
     }
     if (warp == 1) {
         tmem_alloc<1>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -686,11 +909,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_parity = 0;
             bool ok = true, withhold = (p.debug & DEBUG_WITHHOLD_FIRST_LOAD) != 0;
-            WorkIter<STREAM_K> work(p);
-            int t, k0, k1;
-            while (ok && work.next(p, t, k0, k1)) {
-                int mb, nb;
-                tile_coords(p, t, mb, nb);
+            WorkIter<SCHED> work(p);
+            int t, mb, nb, k0, k1;
+            while (ok && work.next(p, t, mb, nb, k0, k1)) {
                 for (int kb = k0; kb < k1; ++kb) {
                     if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, wc, ERR_PRODUCER_SLOT)) {
                         ok = false;
@@ -728,9 +949,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            WorkIter<STREAM_K> work(p);
-            int t, k0, k1;
-            while (ok && work.next(p, t, k0, k1)) {
+            WorkIter<SCHED> work(p);
+            int t, mb, nb, k0, k1;
+            while (ok && work.next(p, t, mb, nb, k0, k1)) {
                 if (!wait_bounded(acce0 + 8u * acc, acc_phase ^ 1u, wc, ERR_MMA_ACCUMULATOR)) {
                     ok = false;
                     break;
@@ -791,80 +1012,158 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         constexpr int64_t SLOT = static_cast<int64_t>(BM) * BN;
         const int64_t my_share = static_cast<int64_t>(ew) * (Cfg::PART_WARP_BYTES / 4);
         uint32_t part_phase = 0;
-        WorkIter<STREAM_K> work(p);
-        int t, k0, k1;
-        while (work.next(p, t, k0, k1)) {
-            int mb, nb;
-            tile_coords(p, t, mb, nb);
-            const uint4 bv = bias_fetch(p, nb * BN, lane);
-            int ok = 1;
-            if (lane == 0)
-                ok = wait_bounded(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok)
-                break;
-            tc_fence_after_sync();
-            const uint32_t tacc = tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c_begin * 32);
-            const int n_first = nb * BN + c_begin * 32, row0 = mb * BM + quarter * 32;
-            if (STREAM_K && k0 > 0) {
-                // a later part of a cut tile: hand the partial sum to the tile's owner
-                epilogue_partial_store<CHUNKS>(p, tacc, p.sk_ws + static_cast<int64_t>(blockIdx.x) * SLOT + my_share,
-                                               n_first, row0, lane);
-                __threadfence();
-                __syncwarp();
-                if (lane == 0)
-                    st_release_gpu_u32(p.sk_flags + blockIdx.x * Cfg::NUM_EPI_WARPS + ew, 1u);
-            } else {
-                int n_parts = 0;
-                if (STREAM_K && k1 < p.num_kb) {
-                    // Owner of a cut tile: the CTAs whose ranges begin inside it hold the rest.
-                    // This is the last part of this CTA's range, so its MMAs are complete and
-                    // the operand ring is idle: each warp pulls a contributor's share into its
-                    // own piece of the ring and adds it to its rows in TMEM.
-                    const int64_t tile_end = static_cast<int64_t>(t + 1) * p.num_kb;
-                    const int g0 = static_cast<int>(blockIdx.x);
-                    while (g0 + n_parts + 1 < static_cast<int>(gridDim.x) && sk_begin(p, g0 + n_parts + 1) < tile_end)
-                        ++n_parts;
-                    const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
-                    const bool inside = valid > 0 && row0 < p.M;
-                    const uint32_t buf = sA + static_cast<uint32_t>(ew * Cfg::PART_WARP_BYTES);
-                    for (int j = 1; ok && j <= n_parts; ++j) {
-                        ok = wait_flag(p.sk_flags + (g0 + j) * Cfg::NUM_EPI_WARPS + ew, wc, lane) ? 1 : 0;
-                        if (!ok || !inside)
-                            continue;
-                        if (lane == 0) {
-                            fence_proxy_async_global();   // acquired data, read next by the copy engine
-                            mbar_arrive_expect_tx(part0 + 8u * ew, Cfg::PART_WARP_BYTES);
-                            bulk_load_g2s(buf, p.sk_ws + static_cast<int64_t>(g0 + j) * SLOT + my_share,
-                                          Cfg::PART_WARP_BYTES, part0 + 8u * ew);
-                            ok = wait_bounded(part0 + 8u * ew, part_phase, wc, ERR_STREAMK_PARTIAL) ? 1 : 0;
-                        }
-                        part_phase ^= 1u;
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (ok)
-                            fold_partial<CHUNKS>(tacc, buf, valid, lane);
-                    }
-                    if (!ok)
+        if constexpr (SCHED == SCHED_ROW_CLUSTER) {
+            // Softmax over a row cluster, pipelined by one tile: pass 1 and the publication of
+            // tile i's row statistics come before the collection and pass 2 of tile i - 1, so
+            // that waiting for the other CTAs overlaps work (both TMEM accumulators hold a tile).
+            // A single CTA per row (N <= 256) has nothing to wait for and finishes each tile at
+            // once, which frees its accumulator for the next MMAs sooner.
+            struct Pending {
+                RowExchange x;
+                uint32_t taddr;
+                int n_first, row0, valid, acc;
+                bool active;
+                float m, s, mc[CHUNKS];
+            };
+            const int row = quarter * 32 + lane;
+            const int group = (warp - 2) >> 2;
+            Pending pend;
+            bool have = false;
+            uint32_t tiles = 0;
+            WorkIter<SCHED> work(p);
+            int t, mb, nb, k0, k1;
+            for (;;) {
+                const bool got = work.next(p, t, mb, nb, k0, k1);
+                Pending cur;
+                if (got) {
+                    const uint4 bv = bias_fetch(p, nb * BN, lane);
+                    int ok = 1;
+                    if (lane == 0)
+                        ok = wait_bounded(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
+                    if (!__shfl_sync(0xffffffffu, ok, 0))
                         break;
+                    tc_fence_after_sync();
+                    if (p.bias != nullptr) {
+                        my_bias[lane] = bv;
+                        __syncwarp();
+                    }
+                    cur.taddr = tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c_begin * 32);
+                    cur.n_first = nb * BN + c_begin * 32;
+                    cur.row0 = mb * BM + quarter * 32;
+                    cur.valid = min(CHUNKS, (p.N - cur.n_first + 31) / 32);
+                    cur.active = cur.valid > 0 && cur.row0 < p.M;
+                    cur.acc = acc;
+                    softmax_pass1<CHUNKS>(p, cur.taddr, cur.n_first, cur.valid, cur.active,
+                                          p.bias != nullptr ? my_bias + c_begin * 4 : nullptr, cur.mc, cur.m, cur.s);
+                    cur.x = RowExchange{base + Cfg::STATS_OFFSET, base + Cfg::PAIR_OFFSET, stats_ready0, stats_read0,
+                                        p.row_cluster, quarter, group, tiles & 1u, tiles >> 1, &wc};
+                    if (!row_publish<Cfg::EPI_COL_GROUPS>(cur.x, cur.m, cur.s, row, lane))
+                        break;
+                    ++tiles;
+                    if (++acc == Cfg::ACC_BUFS) {
+                        acc = 0;
+                        acc_phase ^= 1u;
+                    }
                 }
-                if (p.bias != nullptr) {
-                    my_bias[lane] = bv;
+                auto finish = [&](Pending &f) -> bool {
+                    if (!row_collect(f.x, f.m, f.s, row, lane))
+                        return false;
+                    if (f.active)
+                        softmax_pass2<CHUNKS>(f.taddr, f.n_first, f.row0, f.valid, f.mc, f.m, f.s, &tmap_c, my_stage,
+                                              box_sel, lane);
+                    tc_fence_before_sync();
                     __syncwarp();
-                }
-                epilogue_tile<CHUNKS>(p, tacc, n_first, row0, p.bias != nullptr ? my_bias + c_begin * 4 : nullptr,
-                                      &tmap_c, my_stage, box_sel, lane);
-                if (n_parts > 0 && lane == 0) {   // consumed: lower the flags for the next launch
-                    for (int j = 1; j <= n_parts; ++j)
-                        p.sk_flags[(static_cast<int>(blockIdx.x) + j) * Cfg::NUM_EPI_WARPS + ew] = 0u;
+                    if (lane == 0)
+                        mbar_arrive(acce0 + 8u * f.acc);   // this warp's rows of that accumulator are read
+                    return true;
+                };
+                if (have && !finish(pend))
+                    break;
+                if (!got)
+                    break;
+                if (p.row_cluster == 1) {
+                    if (!finish(cur))
+                        break;
+                    have = false;
+                } else {
+                    pend = cur;
+                    have = true;
                 }
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(acce0 + 8u * acc);   // this warp's rows of the accumulator are read
-            if (++acc == Cfg::ACC_BUFS) {
-                acc = 0;
-                acc_phase ^= 1u;
+        } else {
+            WorkIter<SCHED> work(p);
+            int t, mb, nb, k0, k1;
+            while (work.next(p, t, mb, nb, k0, k1)) {
+                const uint4 bv = bias_fetch(p, nb * BN, lane);
+                int ok = 1;
+                if (lane == 0)
+                    ok = wait_bounded(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                const uint32_t tacc = tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c_begin * 32);
+                const int n_first = nb * BN + c_begin * 32, row0 = mb * BM + quarter * 32;
+                if (SCHED == SCHED_STREAM_K && k0 > 0) {
+                    // a later part of a cut tile: hand the partial sum to the tile's owner
+                    epilogue_partial_store<CHUNKS>(p, tacc, p.sk_ws + static_cast<int64_t>(blockIdx.x) * SLOT + my_share,
+                                                   n_first, row0, lane);
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0)
+                        st_release_gpu_u32(p.sk_flags + blockIdx.x * Cfg::NUM_EPI_WARPS + ew, 1u);
+                } else {
+                    int n_parts = 0;
+                    if (SCHED == SCHED_STREAM_K && k1 < p.num_kb) {
+                        // Owner of a cut tile: the CTAs whose ranges begin inside it hold the rest.
+                        // This is the last part of this CTA's range, so its MMAs are complete and
+                        // the operand ring is idle: each warp pulls a contributor's share into its
+                        // own piece of the ring and adds it to its rows in TMEM.
+                        const int64_t tile_end = static_cast<int64_t>(t + 1) * p.num_kb;
+                        const int g0 = static_cast<int>(blockIdx.x);
+                        while (g0 + n_parts + 1 < static_cast<int>(gridDim.x) && sk_begin(p, g0 + n_parts + 1) < tile_end)
+                            ++n_parts;
+                        const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
+                        const bool inside = valid > 0 && row0 < p.M;
+                        const uint32_t buf = sA + static_cast<uint32_t>(ew * Cfg::PART_WARP_BYTES);
+                        for (int j = 1; ok && j <= n_parts; ++j) {
+                            ok = wait_flag(p.sk_flags + (g0 + j) * Cfg::NUM_EPI_WARPS + ew, wc, lane) ? 1 : 0;
+                            if (!ok || !inside)
+                                continue;
+                            if (lane == 0) {
+                                fence_proxy_async_global();   // acquired data, read next by the copy engine
+                                mbar_arrive_expect_tx(part0 + 8u * ew, Cfg::PART_WARP_BYTES);
+                                bulk_load_g2s(buf, p.sk_ws + static_cast<int64_t>(g0 + j) * SLOT + my_share,
+                                              Cfg::PART_WARP_BYTES, part0 + 8u * ew);
+                                ok = wait_bounded(part0 + 8u * ew, part_phase, wc, ERR_STREAMK_PARTIAL) ? 1 : 0;
+                            }
+                            part_phase ^= 1u;
+                            ok = __shfl_sync(0xffffffffu, ok, 0);
+                            if (ok)
+                                fold_partial<CHUNKS>(tacc, buf, valid, lane);
+                        }
+                        if (!ok)
+                            break;
+                    }
+                    if (p.bias != nullptr) {
+                        my_bias[lane] = bv;
+                        __syncwarp();
+                    }
+                    epilogue_tile<CHUNKS>(p, tacc, n_first, row0, p.bias != nullptr ? my_bias + c_begin * 4 : nullptr,
+                                          &tmap_c, my_stage, box_sel, lane);
+                    if (n_parts > 0 && lane == 0) {   // consumed: lower the flags for the next launch
+                        for (int j = 1; j <= n_parts; ++j)
+                            p.sk_flags[(static_cast<int>(blockIdx.x) + j) * Cfg::NUM_EPI_WARPS + ew] = 0u;
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(acce0 + 8u * acc);   // this warp's rows of the accumulator are read
+                if (++acc == Cfg::ACC_BUFS) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
             }
         }
         if (lane == 0)
@@ -874,6 +1173,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (SCHED == SCHED_ROW_CLUSTER)
+        cluster_sync();   // no CTA leaves while another may still read its statistics
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);

@@ -204,14 +204,68 @@ def test_softmax_epilogue(kctx, shape, with_bias):
     assert np.all(np.abs(C.astype(np.float64).sum(axis=1) - 1) <= N * 2.0 ** -11)
 
 
+WIDE_SOFTMAX = [(300, 264, 128), (129, 1000, 64), (257, 2048, 256), (200, 4096, 128), (4104, 512, 128),
+                (64, 3000, 320), (7, 776, 8)]
+
+
+@pytest.mark.parametrize("shape", WIDE_SOFTMAX, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_softmax_epilogue_wide_rows(ctx, shape, with_bias):
+    """Rows wider than one tile: a cluster of ceil(N/256) CTAs (2 to 16, ragged last tile)
+    per 128-row block exchanges row statistics through distributed shared memory. Same bar
+    as the one-tile softmax: within one FP16 ulp of the oracle, rows sum to 1. 4104 rows =
+    33 row blocks, so clusters loop and reuse both statistics buffers many times."""
+    M, N, K = shape
+    A = inputs.random_fp16((M, K), 6300 + M, "normal")
+    B = inputs.random_fp16((K, N), 6400 + N, "normal_inv_k", k=K)
+    bias = inputs.random_fp16((N,), 6500 + N) if with_bias else None
+    C = run_guarded(ctx, A, B, bias, g.EPI_SOFTMAX).numpy()
+    ref = oracle_ref(A, B, bias, g.EPI_SOFTMAX)
+    ulp = np.maximum(np.spacing(np.abs(ref)).astype(np.float64), 2.0 ** -24)
+    err = np.abs(C.astype(np.float64) - ref.astype(np.float64))
+    assert np.all(np.isfinite(C.astype(np.float64)))
+    assert np.all(err <= ulp), (shape, float(err.max()), int((err > ulp).sum()))
+    assert np.all(np.abs(C.astype(np.float64).sum(axis=1) - 1) <= N * 2.0 ** -11)
+
+
+def test_wide_softmax_timeout_then_recovery(ctx):
+    """Every CTA of every row cluster withholds its first load: the waits (MMA operands,
+    then the row exchange of the others) run out, the kernel returns and reports a timeout,
+    and the context computes a correct wide softmax afterwards."""
+    g.gemm_set_timeout_ns(ctx, 20_000_000)
+    g.gemm_set_debug(ctx, g.GEMM_DEBUG_WITHHOLD_FIRST_LOAD)
+    try:
+        dev = torch.device("cuda:0")
+        A = torch.ones(256, 64, dtype=torch.float16, device=dev)
+        B = torch.ones(64, 1024, dtype=torch.float16, device=dev)
+        C = torch.zeros(256, 1024, dtype=torch.float16, device=dev)
+        g.gemm(ctx, A, B, None, g.EPI_SOFTMAX, out=C)
+        torch.cuda.synchronize()
+        status, detail = g.gemm_last_device_error(ctx)
+        assert status == g.GEMM_ERR_TIMEOUT and detail in (1, 2, 3, 4, 5, 7)
+        assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+    finally:
+        g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
+        g.gemm_set_timeout_ns(ctx, 2_000_000_000)
+    test_softmax_epilogue_wide_rows(ctx, (300, 1000, 64), True)
+
+
 def test_softmax_epilogue_limits(ctx):
     dev = torch.device("cuda:0")
     A = torch.zeros(16, 64, dtype=torch.float16, device=dev)
-    B = torch.zeros(64, 264, dtype=torch.float16, device=dev)
-    C = torch.zeros(16, 264, dtype=torch.float16, device=dev)
-    with pytest.raises(g.GemmError) as e:      # the row does not fit one tile
+    B = torch.zeros(64, 4104, dtype=torch.float16, device=dev)
+    C = torch.zeros(16, 4104, dtype=torch.float16, device=dev)
+    with pytest.raises(g.GemmError) as e:      # 17 tiles per row: more than a cluster holds
         g.gemm(ctx, A, B, None, g.EPI_SOFTMAX, out=C)
     assert e.value.status == g.GEMM_ERR_ARG
+    # K = 0 over a wide row: softmax of the bias
+    bias_w = inputs.random_fp16((1536,), 98).to(dev)
+    Cw = torch.empty(5, 1536, dtype=torch.float16, device=dev)
+    g.gemm_run(ctx, 5, 1536, 0, None, None, bias_w, Cw, g.EPI_SOFTMAX)
+    torch.cuda.synchronize()
+    refw, _ = oracle.softmax_rows(bias_w.cpu()[None, :].repeat(5, 1))
+    ulpw = np.maximum(np.spacing(np.abs(refw)).astype(np.float64), 2.0 ** -24)
+    assert np.all(np.abs(Cw.cpu().numpy().astype(np.float64) - refw.astype(np.float64)) <= ulpw)
     # K = 0: softmax of the bias row; all-zero logits give 1/N everywhere
     bias = inputs.random_fp16((256,), 99).to(dev)
     C2 = torch.empty(3, 256, dtype=torch.float16, device=dev)
