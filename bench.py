@@ -33,7 +33,8 @@ METRIC = "FP16 GEMM TFLOP/s (fp32 acc, ±bias+GELU) and % of GB300 dense FP16 pe
 WORKLOAD = "mlp_up_8200x4096x16384_bias_gelu"
 # Other problems timed briefly in the same run (context lines, not the headline).
 SIDE_WORKLOADS = ["gemm_8192", "gemm_8192_bias_gelu", "mlp_up_8200x4096x16384_none",
-                  "gemm_2048", "gemm_2048_bias_gelu", "gemm_2048_bias_relu", "gemm_256"]
+                  "gemm_2048", "gemm_2048_bias_gelu", "gemm_2048_bias_relu", "gemm_256",
+                  "gemm_1024x1024x8192_bias_gelu"]
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["tensor_core_gemm_tcgen05_gb300/csrc/gemm_kernel.cuh",
@@ -269,34 +270,38 @@ def measure_fused_softmax(g, ctx, stream, device, peaks, steps=30):
     softmax in place: C is written, read and written again)."""
     import torch
     from tensor_core_gemm_tcgen05_gb300 import inputs
-    w = inputs.WORKLOADS["scores_262144x256x128_softmax"]
-    _, (dA, dB, dbias, dC) = device_buffers(w, device)
+    res = {}
+    for wname in ("scores_262144x256x128_softmax", "scores_32768x1024x128_softmax"):
+        w = inputs.WORKLOADS[wname]
+        _, (dA, dB, dbias, dC) = device_buffers(w, device)
 
-    def fused():
-        g.gemm_run(ctx, w.M, w.N, w.K, dA, dB, dbias, dC, g.EPI_SOFTMAX, stream)
+        def fused():
+            g.gemm_run(ctx, w.M, w.N, w.K, dA, dB, dbias, dC, g.EPI_SOFTMAX, stream)
 
-    def unfused():
-        g.gemm_run(ctx, w.M, w.N, w.K, dA, dB, dbias, dC, g.EPI_NONE, stream)
-        g.gemm_row_softmax(ctx, w.M, w.N, dC, dC, stream)
+        def unfused():
+            g.gemm_run(ctx, w.M, w.N, w.K, dA, dB, dbias, dC, g.EPI_NONE, stream)
+            g.gemm_row_softmax(ctx, w.M, w.N, dC, dC, stream)
 
-    out = {}
-    for name, fn in (("fused", fused), ("unfused", unfused)):
-        for _ in range(5):
-            fn()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        out[name] = e0.elapsed_time(e1) / steps * 1e3
-    gbs = w.bytes / (out["fused"] * 1e-6) / 1e9
-    return {w.name: {
-        "us_per_launch": round(out["fused"], 2), "unfused_us": round(out["unfused"], 2),
-        "GB/s": round(gbs, 1), "bound": "hbm", "frac_of_measured_hbm": round(gbs / float(peaks["hbm_gbs"]), 4),
-        "tflops": round(w.flops / (out["fused"] * 1e-6) / 1e12, 1), "algorithmic_bytes_per_launch": w.bytes}}
+        out = {}
+        for name, fn in (("fused", fused), ("unfused", unfused)):
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out[name] = e0.elapsed_time(e1) / steps * 1e3
+        gbs = w.bytes / (out["fused"] * 1e-6) / 1e9
+        res[w.name] = {
+            "us_per_launch": round(out["fused"], 2), "unfused_us": round(out["unfused"], 2),
+            "GB/s": round(gbs, 1), "bound": "hbm", "frac_of_measured_hbm": round(gbs / float(peaks["hbm_gbs"]), 4),
+            "tflops": round(w.flops / (out["fused"] * 1e-6) / 1e12, 1), "algorithmic_bytes_per_launch": w.bytes}
+        del dA, dB, dbias, dC
+    return res
 
 
 ATTN_SHAPE = (64, 4096)   # heads (e.g. batch 4 x 16 heads) and tokens, head dimension 128
