@@ -10,35 +10,28 @@
 // per block; "Designing High-Performance GPU Kernels with TileLang" on spaxe.top: causal and
 // non-causal). Built on the same fifth-generation tensor-core machinery as the GEMM:
 //
-//  * one CTA per (head, block of 128 queries); the blocks with the most keys (causal) start
-//    first;
-//  * warp 0: TMA producer. Q once (two 128-byte-swizzled K-major atoms of 64 head dims), then
-//    K and V blocks of 128 keys through a two-stage ring; 3-D tensor maps [head][row][dim] so
-//    rows past the sequence read as zero;
-//  * warp 1: MMA issuer. S_j = Q K_j^T (M = N = 128, K = 128, both operands K-major) into one
-//    of two TMEM score buffers, so that S_{j+1} is computed while the softmax of block j
-//    runs; then O += P_j V_j (P K-major from shared memory, V MN-major) into a TMEM FP32
-//    accumulator;
-//  * warps 2..5: online softmax. Each thread owns one query row (its TMEM lane). Per block it
-//    reads its 128 scores from TMEM, takes the row maximum, rescales the row of O in TMEM by
-//    exp(m_old - m_new) when the maximum grew, writes p = exp(s - m_new) as FP16 into the
-//    shared-memory P tile (the K-major 128-byte-swizzled layout the MMA reads) and keeps the
-//    running sum l; at the end it writes O / l.
+//  * one CTA per (head, block of 256 queries) = two query tiles A and B of 128 rows; the
+//    blocks with the most keys (causal) start first;
+//  * warp 0: TMA producer. Both Q tiles once (K-major, two 128-byte-swizzled atoms of 64 head
+//    dims each), then K and V blocks of 128 keys through a two-stage ring; 3-D tensor maps
+//    [head][row][dim] so that rows past the sequence read as zero;
+//  * warp 1: MMA issuer. S_t = Q_t K_j^T (M = N = 128, K = 128, both operands K-major from
+//    shared memory) into tile t's TMEM score columns; O_t += P_t V_j with P_t read from Tensor
+//    Memory (written by the softmax over the first half of the score columns, FP16 pairs)
+//    and V MN-major from shared memory. Issue order per key block j: P_A V_j, S_A for block
+//    j + 1, P_B V_j, S_B for block j + 1, so that the tensor cores work on one tile while
+//    the other tile's softmax runs;
+//  * warps 2..5 (tile A) and 6..9 (tile B): online softmax, one query row per thread (its
+//    TMEM lane). Per block: the row maximum of the scores; when it exceeds the running
+//    maximum by more than kRescaleThreshold, the row of O is rescaled in TMEM (after the
+//    previous P V product); p = 2^(s * scale * log2(e) - m) written as FP16 over the scores
+//    (the A operand of P V), summed into the running denominator l. At the end: O / l.
 // Every mbarrier wait is bounded in time, as in the GEMM kernels.
 #pragma once
 
 #include "gemm_kernel.cuh"
 
 namespace gb300 {
-
-// 2^x with the MUFU.EX2 instruction (flushes denormal results to zero, which only affects
-// probabilities below 2^-126, far under FP16's smallest value).
-__device__ __forceinline__ float fast_exp2(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 // A row's running maximum is raised (and its row of O rescaled) only when a block's maximum
 // exceeds it by more than this many base-2 units; otherwise probabilities are taken against
@@ -48,7 +41,7 @@ constexpr float kRescaleThreshold = 8.0f;
 struct AttnParams {
     int H;              // heads (batch x heads)
     int Sq, Sk;         // query and key lengths
-    int q_blocks;       // ceil(Sq / 128)
+    int q_blocks;       // ceil(Sq / 256): CTAs per head
     int causal;
     float scale_log2;   // scale * log2(e): scores are kept in base-2 units
     __half *O;          // [H][Sq][128]
@@ -58,26 +51,27 @@ struct AttnParams {
 
 struct AttnConfig {
     static constexpr int D = 128;         // head dimension
-    static constexpr int BQ = 128;        // queries per CTA (= TMEM lanes)
+    static constexpr int BQ = 128;        // queries per tile (= TMEM lanes)
+    static constexpr int TILES = 2;       // query tiles per CTA
     static constexpr int BKV = 128;       // keys per block
     static constexpr int ATOM_BYTES = 128 * 128;   // 128 rows x 64 FP16 (one 128-byte swizzle row each)
     static constexpr int TILE_BYTES = 2 * ATOM_BYTES;  // 128 x 128 FP16
     static constexpr int KV_STAGES = 2;
-    // shared memory: Q | K[0] V[0] | K[1] V[1] | P | barriers
+    // shared memory: Q_A Q_B | K[0] V[0] | K[1] V[1] | barriers
     static constexpr int Q_OFF = 0;
-    static constexpr int KV_OFF = TILE_BYTES;
-    static constexpr int P_OFF = KV_OFF + KV_STAGES * 2 * TILE_BYTES;
-    static constexpr int BAR_OFF = P_OFF + TILE_BYTES;
-    // barriers: q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, pv_done, drain
-    static constexpr int NUM_BARS = 1 + 2 * KV_STAGES + 2 * 2 + 3;
+    static constexpr int KV_OFF = TILES * TILE_BYTES;
+    static constexpr int BAR_OFF = KV_OFF + KV_STAGES * 2 * TILE_BYTES;
+    // barriers: q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2], drain
+    static constexpr int NUM_BARS = 1 + 2 * KV_STAGES + 3 * TILES + 1;
     static constexpr int SMEM_BYTES = 1024 + BAR_OFF + NUM_BARS * 8 + 16;
-    static constexpr int NUM_THREADS = 192;
-    static constexpr int TMEM_COLS = 512;   // S0 | S1 | O (128 columns each)
+    static constexpr int NUM_THREADS = 64 + TILES * 128;
+    // TMEM: S_A | S_B | O_A | O_B, 128 columns each; P_t over the first 64 columns of S_t
+    static constexpr int TMEM_COLS = 512;
     static constexpr int S_COL = 0, O_COL = 256;
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 };
 
-// Instruction descriptor, kind::f16, FP32 accumulate, FP16 operands, M = N = 128.
+// Instruction descriptor, kind::f16, FP32 accumulate, FP16 operands, M = N = 128, A K-major.
 // b_mn_major: B is MN-major (V, head dims contiguous) instead of K-major (K, keys' dims
 // contiguous).
 template <bool B_MN_MAJOR>
@@ -124,45 +118,55 @@ __device__ __forceinline__ void two_buffered_chunks(uint32_t addr, uint32_t (&va
     fn(vb, 3);
 }
 
-// Online softmax of one epilogue warp (warps 2..5): each thread owns query row r of the
-// block (TMEM lane r). Per key block j: (1) read the 128 scores of the row and take their
-// maximum (base-2 units; keys past the sequence, or after the query when causal, are left
-// out); (2) once the previous P V product has finished, rescale the row of O in TMEM by
-// 2^(m_old - m_new) if the maximum grew by more than kRescaleThreshold (skipped when no row
-// of the warp needs it); (3) read
-// the scores again and write p = 2^(s - m_new) as FP16 into the P tile, K-major with the
-// 128-byte swizzle (16-byte piece c of row r at atom (c / 8), r * 128 + ((c % 8) ^ (r % 8)) * 16),
-// summing p into the running denominator l. At the end the row of O is divided by l.
-__device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint32_t tmem, uint32_t sP,
-                                                       uint32_t s_full0, uint32_t s_empty0, uint32_t p_full,
-                                                       uint32_t pv_done, const WaitCtl &wc, int warp, int lane,
-                                                       int q0, int h, int n_kv)
+// Online softmax of one warp of tile t's softmax group: each thread owns query row r of the
+// tile (TMEM lane r). Per key block j: (1) read the 128 scores of the row and take their
+// maximum in base-2 units (keys past the sequence, or after the query when causal, are left
+// out); (2) if the maximum grew by more than kRescaleThreshold for some row of the warp, wait
+// for the previous P V product of this tile and rescale the warp's rows of O by
+// 2^(m_old - m_new); (3) read the scores again and write p = 2^(s - m_new) as FP16 pairs over
+// the first 64 score columns (chunk c of 32 keys to columns 16c..16c+15: each lies in score
+// columns that were already read), summing p into the running denominator l. At the end the
+// row of O is divided by l and stored.
+__device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint32_t tmem, int tile, uint32_t s_full,
+                                                       uint32_t p_full, uint32_t pv_done, const WaitCtl &wc, int warp,
+                                                       int lane, int q0, int h, int n_kv)
 {
     using Cfg = AttnConfig;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int qi = q0 + r;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t o_addr = tmem + lane_base + Cfg::O_COL;
+    const uint32_t s_addr = tmem + lane_base + static_cast<uint32_t>(Cfg::S_COL + tile * Cfg::BQ);
+    const uint32_t o_addr = tmem + lane_base + static_cast<uint32_t>(Cfg::O_COL + tile * Cfg::D);
     const int kmax = p.causal ? min(p.Sk - 1, qi) : p.Sk - 1;   // last key this row sees
+    const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.0f;
     uint32_t v[32], va[32], vb[32];
     for (int j = 0; j < n_kv; ++j) {
-        const int b = j & 1;
         int w = 1;
         if (lane == 0)
-            w = wait_bounded(s_full0 + 8u * b, static_cast<uint32_t>(j >> 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
+            w = wait_bounded(s_full, static_cast<uint32_t>(j) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w, 0))
             return;
         tc_fence_after_sync();
-        const uint32_t s_addr = tmem + lane_base + Cfg::S_COL + static_cast<uint32_t>(b) * 128u;
         const int k0 = j * Cfg::BKV;
+        const bool full = k0 + Cfg::BKV - 1 <= kmax;   // no key of the block is masked for this row
         float mb = -INFINITY;
         auto max_chunk = [&](const uint32_t(&x)[32], int c) {
+            if (full) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const float t = __uint_as_float(x[e]) * p.scale_log2;
-                mb = (k0 + 32 * c + e <= kmax) ? fmaxf(mb, t) : mb;
+                for (int e = 0; e < 32; e += 2) {
+                    float a, b;
+                    f32x2_unpack(f32x2_mul(f32x2_pack(__uint_as_float(x[e]), __uint_as_float(x[e + 1])),
+                                           f32x2_pack(sl2, sl2)),
+                                 a, b);
+                    mb = fmaxf(mb, fmaxf(a, b));
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (k0 + 32 * c + e <= kmax)
+                        mb = fmaxf(mb, __uint_as_float(x[e]) * sl2);
             }
         };
         two_buffered_chunks(s_addr, va, vb, max_chunk);
@@ -170,59 +174,63 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
         const bool raise = mb > m + kRescaleThreshold || m == -INFINITY;
         const float m_new = raise ? mb : m;
         const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-        const float alpha = raise ? fast_exp2(m - m_use) : 1.0f;   // 0 on the first block (m = -inf)
-        if (j > 0) {
+        const float alpha = raise ? ex2_approx(m - m_use) : 1.0f;   // 0 on the first block (m = -inf)
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+            // P_t V of block j - 1 is pv_done's completion number j - 1
             if (lane == 0)
                 w = wait_bounded(pv_done, static_cast<uint32_t>(j - 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
             if (!__shfl_sync(0xffffffffu, w, 0))
                 return;
             tc_fence_after_sync();
-            if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld_32x32b_x32(o_addr + 32u * c, v);
-                    tmem_ld_wait_regs(v);
+            for (int c = 0; c < 4; ++c) {
+                tmem_ld_32x32b_x32(o_addr + 32u * c, v);
+                tmem_ld_wait_regs(v);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st_32x32b_x32(o_addr + 32u * c, v);
-                    tmem_st_wait();
+                for (int e = 0; e < 32; e += 2) {
+                    float a, b;
+                    f32x2_unpack(f32x2_mul(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                           f32x2_pack(alpha, alpha)),
+                                 a, b);
+                    v[e] = __float_as_uint(a);
+                    v[e + 1] = __float_as_uint(b);
                 }
+                tmem_st_32x32b_x32(o_addr + 32u * c, v);
             }
+            tmem_st_wait();
         }
-        float sum = 0.0f;
+        uint64_t sum2 = f32x2_pack(0.0f, 0.0f);
+        const uint64_t scale2 = f32x2_pack(sl2, sl2), neg_m2 = f32x2_pack(-m_use, -m_use);
         auto p_chunk = [&](const uint32_t(&x)[32], int c) {
+            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int idx = 8 * i + 2 * e;
-                    const int k = k0 + 32 * c + idx;
-                    const float p0 = k <= kmax ? fast_exp2(fmaf(__uint_as_float(x[idx]), p.scale_log2, -m_use)) : 0.0f;
-                    const float p1 =
-                        k + 1 <= kmax ? fast_exp2(fmaf(__uint_as_float(x[idx + 1]), p.scale_log2, -m_use)) : 0.0f;
-                    sum += p0 + p1;
-                    __half2 hh = __floats2half2_rn(p0, p1);
-                    pk[e] = *reinterpret_cast<uint32_t *>(&hh);
+            for (int i = 0; i < 16; ++i) {
+                float t0, t1;
+                f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])), scale2,
+                                       neg_m2),
+                             t0, t1);
+                float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+                if (!full) {
+                    const int k = k0 + 32 * c + 2 * i;
+                    p0 = k <= kmax ? p0 : 0.0f;
+                    p1 = k + 1 <= kmax ? p1 : 0.0f;
                 }
-                const int kc = 4 * c + i;   // 16-byte piece of the row: keys 8kc .. 8kc+7
-                const uint32_t addr = sP + static_cast<uint32_t>(kc >> 3) * Cfg::ATOM_BYTES +
-                                      static_cast<uint32_t>(r) * 128u +
-                                      ((static_cast<uint32_t>(kc & 7) ^ static_cast<uint32_t>(r & 7)) << 4);
-                st_shared_v4(addr, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                sum2 = f32x2_add(sum2, f32x2_pack(p0, p1));
+                __half2 hh = __floats2half2_rn(p0, p1);
+                pk[i] = *reinterpret_cast<uint32_t *>(&hh);
             }
+            tmem_st_32x32b_x16(s_addr + 16u * static_cast<uint32_t>(c), pk);   // P over read scores
         };
         two_buffered_chunks(s_addr, va, vb, p_chunk);
-        l = l * alpha + sum;
+        float s0, s1;
+        f32x2_unpack(sum2, s0, s1);
+        l = l * alpha + (s0 + s1);
         m = m_new;
-        fence_proxy_async_shared();   // P is read by the tensor cores (async proxy)
+        tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(s_empty0 + 8u * b);   // score buffer b may be overwritten
-            mbar_arrive(p_full);              // P tile ready, O rescaled
-        }
+        if (lane == 0)
+            mbar_arrive(p_full);   // P_t written (and O_t rescaled): the MMA warp may multiply
     }
     if (n_kv == 0)
         return;
@@ -264,21 +272,24 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *sp = smem_raw + (base - raw);
-    const uint32_t sQ = base + Cfg::Q_OFF, sKV = base + Cfg::KV_OFF, sP = base + Cfg::P_OFF;
+    const uint32_t sQ = base + Cfg::Q_OFF, sKV = base + Cfg::KV_OFF;
+    // barrier k lives at bar0 + 8k: q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2],
+    // pv_done[2], drain (index [t] = query tile)
     const uint32_t q_full = base + Cfg::BAR_OFF;
     const uint32_t kv_full0 = q_full + 8u, kv_empty0 = kv_full0 + 8u * Cfg::KV_STAGES;
-    const uint32_t s_full0 = kv_empty0 + 8u * Cfg::KV_STAGES, s_empty0 = s_full0 + 16u;
-    const uint32_t p_full = s_empty0 + 16u, pv_done = p_full + 8u, drain = pv_done + 8u;
+    const uint32_t s_full0 = kv_empty0 + 8u * Cfg::KV_STAGES, p_full0 = s_full0 + 8u * Cfg::TILES;
+    const uint32_t pv_done0 = p_full0 + 8u * Cfg::TILES, drain = pv_done0 + 8u * Cfg::TILES;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sp + Cfg::BAR_OFF + Cfg::NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // work item: query block qb of head h; the blocks with the most keys go first
+    // work item: query block qb (256 queries, two tiles) of head h; the blocks with the most
+    // keys go first
     const int qb = p.q_blocks - 1 - static_cast<int>(blockIdx.x / static_cast<unsigned>(p.H));
     const int h = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.H));
-    const int q0 = qb * Cfg::BQ;
-    const int k_end = p.causal ? min(p.Sk, q0 + Cfg::BQ) : p.Sk;   // keys any row of the block may see
+    const int q0 = qb * Cfg::TILES * Cfg::BQ;
+    const int k_end = p.causal ? min(p.Sk, q0 + Cfg::TILES * Cfg::BQ) : p.Sk;   // keys any row may see
     const int n_kv = (k_end + Cfg::BKV - 1) / Cfg::BKV;
 
     if (threadIdx.x == 0) {
@@ -287,12 +298,11 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
             mbar_init(kv_full0 + 8u * s, 1);
             mbar_init(kv_empty0 + 8u * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(s_full0 + 8u * b, 1);
-            mbar_init(s_empty0 + 8u * b, 4);
+        for (int t = 0; t < Cfg::TILES; ++t) {
+            mbar_init(s_full0 + 8u * t, 1);
+            mbar_init(p_full0 + 8u * t, 4);   // the four softmax warps of tile t
+            mbar_init(pv_done0 + 8u * t, 1);
         }
-        mbar_init(p_full, 4);
-        mbar_init(pv_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -315,9 +325,11 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, TILE);
-            tma_load_3d(sQ, &tmap_q, q_full, 0, q0, h);
-            tma_load_3d(sQ + ATOM, &tmap_q, q_full, 64, q0, h);
+            mbar_arrive_expect_tx(q_full, Cfg::TILES * TILE);
+            for (int t = 0; t < Cfg::TILES; ++t) {
+                tma_load_3d(sQ + t * TILE, &tmap_q, q_full, 0, q0 + t * Cfg::BQ, h);
+                tma_load_3d(sQ + t * TILE + ATOM, &tmap_q, q_full, 64, q0 + t * Cfg::BQ, h);
+            }
             bool ok = true;
             uint32_t issued = 0, issued_parity = 0;
             for (int j = 0; j < n_kv; ++j) {
@@ -350,42 +362,70 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t ID_QK = idesc_attn<false>(), ID_PV = idesc_attn<true>();
             bool ok = wait_bounded(q_full, 0, wc, ERR_MMA_OPERANDS);
-            // S_j = Q K_j^T into score buffer j % 2
-            auto issue_qk = [&](int j) -> bool {
-                const int s = j & 1;
-                const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-                if (!wait_bounded(kv_full0 + 8u * s, ph, wc, ERR_MMA_OPERANDS))
-                    return false;
-                if (!wait_bounded(s_empty0 + 8u * s, ph ^ 1u, wc, ERR_MMA_ACCUMULATOR))
-                    return false;
-                tc_fence_after_sync();
-                const uint32_t sK = sKV + static_cast<uint32_t>(s) * 2u * TILE;
-                const uint32_t d = tmem + Cfg::S_COL + static_cast<uint32_t>(s) * 128u;
+            // S_t = Q_t K_j^T into tile t's score columns
+            auto issue_qk = [&](int t, int j) {
+                const uint32_t sK = sKV + static_cast<uint32_t>(j & 1) * 2u * TILE;
+                const uint32_t d = tmem + static_cast<uint32_t>(Cfg::S_COL + t * Cfg::BQ);
 #pragma unroll
                 for (int kk = 0; kk < Cfg::D / 16; ++kk)
-                    umma_f16<1>(d, kmajor_step_desc(sQ, kk), kmajor_step_desc(sK, kk), ID_QK, kk != 0 ? 1u : 0u);
-                umma_commit(s_full0 + 8u * s);
-                return true;
+                    umma_f16<1>(d, kmajor_step_desc(sQ + t * TILE, kk), kmajor_step_desc(sK, kk), ID_QK,
+                                kk != 0 ? 1u : 0u);
+                umma_commit(s_full0 + 8u * t);
             };
-            if (ok && n_kv > 0)
-                ok = issue_qk(0);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv && !issue_qk(j + 1)) {   // the next scores overlap this softmax
-                    ok = false;
-                    break;
-                }
-                if (!wait_bounded(p_full, static_cast<uint32_t>(j) & 1u, wc, ERR_MMA_OPERANDS)) {
-                    ok = false;
-                    break;
-                }
+            // O_t += P_t V_j, P_t from TMEM (8 columns per 16 keys)
+            auto issue_pv = [&](int t, int j) -> bool {
+                if (!wait_bounded(p_full0 + 8u * t, static_cast<uint32_t>(j) & 1u, wc, ERR_MMA_OPERANDS))
+                    return false;
                 tc_fence_after_sync();
                 const uint32_t sV = sKV + static_cast<uint32_t>(j & 1) * 2u * TILE + TILE;
+                const uint32_t d = tmem + static_cast<uint32_t>(Cfg::O_COL + t * Cfg::D);
+                const uint32_t a = tmem + static_cast<uint32_t>(Cfg::S_COL + t * Cfg::BQ);
 #pragma unroll
                 for (int kk = 0; kk < Cfg::BKV / 16; ++kk)
-                    umma_f16<1>(tmem + Cfg::O_COL, kmajor_step_desc(sP, kk), v_step_desc(sV, kk), ID_PV,
-                                (j | kk) != 0 ? 1u : 0u);
-                umma_commit(pv_done);                   // O updated, P tile free
-                umma_commit(kv_empty0 + 8u * (j & 1));  // K_j and V_j consumed
+                    umma_f16_tmem_a(d, a + 8u * static_cast<uint32_t>(kk), v_step_desc(sV, kk), ID_PV,
+                                    (j | kk) != 0 ? 1u : 0u);
+                umma_commit(pv_done0 + 8u * t);
+                return true;
+            };
+            // the next S_t overwrites P_t: only once this tile's P V product has finished
+            auto next_qk = [&](int t, int j) -> bool {
+                if (!wait_bounded(pv_done0 + 8u * t, static_cast<uint32_t>(j) & 1u, wc, ERR_MMA_ACCUMULATOR))
+                    return false;
+                tc_fence_after_sync();
+                issue_qk(t, j + 1);
+                return true;
+            };
+            if (ok && n_kv > 0) {
+                ok = wait_bounded(kv_full0, 0, wc, ERR_MMA_OPERANDS);
+                if (ok) {
+                    tc_fence_after_sync();
+                    issue_qk(0, 0);
+                    issue_qk(1, 0);
+                }
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const bool more = j + 1 < n_kv;
+                if (!issue_pv(0, j)) {
+                    ok = false;
+                    break;
+                }
+                if (more) {
+                    const int s = (j + 1) & 1;
+                    if (!wait_bounded(kv_full0 + 8u * s, static_cast<uint32_t>((j + 1) >> 1) & 1u, wc, ERR_MMA_OPERANDS) ||
+                        !next_qk(0, j)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!issue_pv(1, j)) {
+                    ok = false;
+                    break;
+                }
+                umma_commit(kv_empty0 + 8u * (j & 1));   // K_j and V_j consumed by both tiles
+                if (more && !next_qk(1, j)) {
+                    ok = false;
+                    break;
+                }
             }
             if (!ok) {
                 umma_commit(drain);
@@ -395,7 +435,9 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------------------------- online softmax
-        attention_softmax_warp(p, tmem, sP, s_full0, s_empty0, p_full, pv_done, wc, warp, lane, q0, h, n_kv);
+        const int t = (warp - 2) >> 2;   // warps 2..5: tile A, 6..9: tile B
+        attention_softmax_warp(p, tmem, t, s_full0 + 8u * t, p_full0 + 8u * t, pv_done0 + 8u * t, wc, warp, lane,
+                               q0 + t * Cfg::BQ, h, n_kv);
     }
 
     tc_fence_before_sync();

@@ -670,7 +670,7 @@ int gemm_attention_fwd(gemm_ctx *ctx, int64_t heads, int64_t seq_q, int64_t seq_
     const size_t qb = static_cast<size_t>(heads) * seq_q * Cfg::D * 2, kb = static_cast<size_t>(heads) * seq_k * Cfg::D * 2;
     if (overlaps(O, qb, Q, qb) || overlaps(O, qb, K, kb) || overlaps(O, qb, V, kb))
         return GEMM_ERR_ARG;
-    const int64_t q_blocks = (seq_q + Cfg::BQ - 1) / Cfg::BQ;
+    const int64_t q_blocks = (seq_q + Cfg::TILES * Cfg::BQ - 1) / (Cfg::TILES * Cfg::BQ);
     if (heads * q_blocks > INT32_MAX)
         return GEMM_ERR_ARG;
     if (!on_device(Q, ctx->device) || !on_device(K, ctx->device) || !on_device(V, ctx->device) ||
