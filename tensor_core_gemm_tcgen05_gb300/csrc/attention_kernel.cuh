@@ -151,16 +151,29 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
         tc_fence_after_sync();
         const int k0 = j * Cfg::BKV;
         const bool full = k0 + Cfg::BKV - 1 <= kmax;   // no key of the block is masked for this row
+        // Block maximum of scale * s (base-2 units). On unmasked blocks: the maximum (minimum
+        // for a negative scale) of the raw scores in four independent three-input chains,
+        // scaled once.
         float mb = -INFINITY;
+        float r0 = sl2 >= 0.0f ? -INFINITY : INFINITY, r1 = r0, r2 = r0, r3 = r0;
         auto max_chunk = [&](const uint32_t(&x)[32], int c) {
             if (full) {
+                if (sl2 >= 0.0f) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float a, b;
-                    f32x2_unpack(f32x2_mul(f32x2_pack(__uint_as_float(x[e]), __uint_as_float(x[e + 1])),
-                                           f32x2_pack(sl2, sl2)),
-                                 a, b);
-                    mb = fmaxf(mb, fmaxf(a, b));
+                    for (int e = 0; e < 32; e += 8) {
+                        r0 = fmax3(r0, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+                        r1 = fmax3(r1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
+                        r2 = fmax3(r2, __uint_as_float(x[e + 4]), __uint_as_float(x[e + 5]));
+                        r3 = fmax3(r3, __uint_as_float(x[e + 6]), __uint_as_float(x[e + 7]));
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        r0 = fmin3(r0, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+                        r1 = fmin3(r1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
+                        r2 = fmin3(r2, __uint_as_float(x[e + 4]), __uint_as_float(x[e + 5]));
+                        r3 = fmin3(r3, __uint_as_float(x[e + 6]), __uint_as_float(x[e + 7]));
+                    }
                 }
             } else {
 #pragma unroll
@@ -170,6 +183,8 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
             }
         };
         two_buffered_chunks(s_addr, va, vb, max_chunk);
+        if (full)
+            mb = (sl2 >= 0.0f ? fmax3(fmaxf(r0, r1), r2, r3) : fmin3(fminf(r0, r1), r2, r3)) * sl2;
         // keep the old maximum unless this block's exceeds it by more than the threshold
         const bool raise = mb > m + kRescaleThreshold || m == -INFINITY;
         const float m_new = raise ? mb : m;
@@ -199,7 +214,9 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
             }
             tmem_st_wait();
         }
-        uint64_t sum2 = f32x2_pack(0.0f, 0.0f);
+        // four independent packed partial sums
+        uint64_t sum2[4] = {f32x2_pack(0.0f, 0.0f), f32x2_pack(0.0f, 0.0f), f32x2_pack(0.0f, 0.0f),
+                            f32x2_pack(0.0f, 0.0f)};
         const uint64_t scale2 = f32x2_pack(sl2, sl2), neg_m2 = f32x2_pack(-m_use, -m_use);
         auto p_chunk = [&](const uint32_t(&x)[32], int c) {
             uint32_t pk[16];
@@ -215,7 +232,7 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
                     p0 = k <= kmax ? p0 : 0.0f;
                     p1 = k + 1 <= kmax ? p1 : 0.0f;
                 }
-                sum2 = f32x2_add(sum2, f32x2_pack(p0, p1));
+                sum2[i & 3] = f32x2_add(sum2[i & 3], f32x2_pack(p0, p1));
                 __half2 hh = __floats2half2_rn(p0, p1);
                 pk[i] = *reinterpret_cast<uint32_t *>(&hh);
             }
@@ -223,7 +240,7 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
         };
         two_buffered_chunks(s_addr, va, vb, p_chunk);
         float s0, s1;
-        f32x2_unpack(sum2, s0, s1);
+        f32x2_unpack(f32x2_add(f32x2_add(sum2[0], sum2[1]), f32x2_add(sum2[2], sum2[3])), s0, s1);
         l = l * alpha + (s0 + s1);
         m = m_new;
         tmem_st_wait();

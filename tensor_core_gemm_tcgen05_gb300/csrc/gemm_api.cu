@@ -677,19 +677,21 @@ int gemm_attention_fwd(gemm_ctx *ctx, int64_t heads, int64_t seq_q, int64_t seq_
         !on_device(O, ctx->device))
         return GEMM_ERR_DEVICE;
     DeviceGuard guard(ctx->device);
-    // [head][row][dim] views, 64 x 128 boxes (64 dims = one 128-byte swizzle row, 128 rows)
-    auto encode_3d = [&](CUtensorMap *map, const void *ptr, int64_t rows) {
+    // [head][row][dim] views, boxes of 64 dims (one 128-byte swizzle row) x box_rows rows:
+    // 128 query rows (a query tile), 64 key rows (a key block)
+    auto encode_3d = [&](CUtensorMap *map, const void *ptr, int64_t rows, uint32_t box_rows) {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(Cfg::D), static_cast<cuuint64_t>(rows),
                                     static_cast<cuuint64_t>(heads)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Cfg::D) * 2, static_cast<cuuint64_t>(rows) * Cfg::D * 2};
-        const cuuint32_t box[3] = {64, 128, 1};
+        const cuuint32_t box[3] = {64, box_rows, 1};
         const cuuint32_t estr[3] = {1, 1, 1};
         return ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
     CUtensorMap tq, tk, tv;
-    if (!encode_3d(&tq, Q, seq_q) || !encode_3d(&tk, K, seq_k) || !encode_3d(&tv, V, seq_k))
+    if (!encode_3d(&tq, Q, seq_q, Cfg::BQ) || !encode_3d(&tk, K, seq_k, Cfg::BKV) ||
+        !encode_3d(&tv, V, seq_k, Cfg::BKV))
         return GEMM_ERR_LAUNCH;
     gb300::AttnParams p;
     p.H = static_cast<int>(heads);

@@ -486,6 +486,21 @@ __device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b)
     return d;
 }
 
+// max(a, b, c) and min(a, b, c) in one instruction each.
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float fmin3(float a, float b, float c)
+{
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // 1/x and 2^x on the special-function unit (approximate: about one and two units in the last
 // place; denormal inputs and results flushed to zero).
 __device__ __forceinline__ float rcp_approx(float x)

@@ -88,6 +88,39 @@ def test_attention_long_sequence_sampled_rows(ctx):
         check(got, ref, f"S=4096 causal={causal}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_full_size_every_head(ctx, causal):
+    """The benchmark's shape, 64 heads x 4096 tokens: a full grid of CTAs, so that races
+    between the kernel's warps (which small grids can hide) show. Every head against the
+    FP64 oracle on sampled rows, and every row against plain FP32 PyTorch arithmetic on the
+    GPU (softmax of the FP32 scores, times V): same elementwise bar."""
+    H, S = 64, 4096
+    Q, K, V = qkv(H, S, S, 17)
+    scale = 1.0 / math.sqrt(D)
+    O = run(ctx, Q, K, V, scale, causal)
+    rows = [(h, int(i)) for h in range(H) for i in inputs.sample_rows(S, 4, seed=100 + h, include_last=1)]
+    ref, _ = oracle.attention(Q, K, V, scale, causal, rows=rows)
+    check(np.stack([O[h, i].numpy() for h, i in rows]), ref, f"every head, causal={causal}")
+    dev = torch.device("cuda:0")
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        mask = torch.ones(S, S, dtype=torch.bool, device=dev).tril() if causal else None
+        worst = 0.0
+        for h in range(H):
+            s_ = (Q[h].to(dev).float() @ K[h].to(dev).float().T) * scale
+            if mask is not None:
+                s_ = s_.masked_fill(~mask, float("-inf"))
+            ref_h = torch.softmax(s_, dim=1) @ V[h].to(dev).float()
+            err = (O[h].to(dev).float() - ref_h).abs()
+            bad = err > 3e-3 + 4e-3 * ref_h.abs()
+            assert not bool(bad.any()), (h, int(bad.sum()), float(err.max()))
+            worst = max(worst, float(err.max()))
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    assert worst < 3e-3
+
+
 def test_attention_special_cases(ctx):
     H, S = 2, 384
     _, K, V = qkv(H, S, S, 31)
