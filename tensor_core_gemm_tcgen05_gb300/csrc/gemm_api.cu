@@ -25,9 +25,11 @@ using Cfg = gb300::KernelConfig<128, 256, 4, GB300_EPI_WARPS>;
 #define GB300_PAIR_STAGES 6
 #endif
 using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS>;
-// The softmax epilogue's kernel: the same 128 x 256 tiles, a shorter ring (softmax GEMMs have
-// small K) and eight epilogue warps, two per TMEM lane quarter, each with half of the columns.
-using SmCfg = gb300::KernelConfig<128, 256, 3, 8>;
+// The same 128 x 256 tiles with a shorter ring and eight epilogue warps (two per TMEM lane
+// quarter, each with half of the columns): the softmax epilogue's kernel (softmax GEMMs have
+// small K), and the whole-tile kernel when all tiles fit one wave, where every CTA's
+// epilogue is an exposed tail that twice the warps shorten (2048^3: 15.6 -> 15.0 us).
+using Cfg8 = gb300::KernelConfig<128, 256, 3, 8>;
 #ifndef GB300_GROUP_PANEL_MB
 #define GB300_GROUP_PANEL_MB 32
 #endif
@@ -266,17 +268,17 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     // least one; otherwise 128 x 256 tiles on single SMs (twice as many tiles to spread).
     if (epilogue == GEMM_EPI_SOFTMAX) {
         // one cluster of n_blocks CTAs (a single CTA when N <= 256) per 128-row block
-        static_assert(SmCfg::BM == Cfg::BM && SmCfg::BN == Cfg::BN && SmCfg::BK == Cfg::BK &&
-                          SmCfg::B_BOX_N == Cfg::B_BOX_N,
+        static_assert(Cfg8::BM == Cfg::BM && Cfg8::BN == Cfg::BN && Cfg8::BK == Cfg::BK &&
+                          Cfg8::B_BOX_N == Cfg::B_BOX_N,
                       "same tensor-map boxes as the GEMM kernel");
-        p.m_blocks = (M + SmCfg::BM - 1) / SmCfg::BM;
-        p.n_blocks = (N + SmCfg::BN - 1) / SmCfg::BN;
+        p.m_blocks = (M + Cfg8::BM - 1) / Cfg8::BM;
+        p.n_blocks = (N + Cfg8::BN - 1) / Cfg8::BN;
         p.num_tiles = p.m_blocks * p.n_blocks;
         p.group_m = 1;
         p.row_cluster = p.n_blocks;
         const int clusters = std::min(p.m_blocks, ctx->row_clusters[p.n_blocks]);
-        launch_pdl_cluster(gb300::gemm_tcgen05_kernel<SmCfg, gb300::SCHED_ROW_CLUSTER>, clusters * p.n_blocks,
-                           p.n_blocks, SmCfg::NUM_THREADS, SmCfg::SMEM_BYTES, stream, ta, tb, tc, p);
+        launch_pdl_cluster(gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_ROW_CLUSTER>, clusters * p.n_blocks,
+                           p.n_blocks, Cfg8::NUM_THREADS, Cfg8::SMEM_BYTES, stream, ta, tb, tc, p);
         const cudaError_t e = cudaGetLastError();
         return e == cudaSuccess ? GEMM_OK : cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
     }
@@ -316,9 +318,18 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
                 grid = g_sk;
             }
         }
-        launch_pdl(p.sk_units > 0 ? gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_STREAM_K>
-                                  : gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_TILES>,
-                   grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
+        static_assert(Cfg8::BM == Cfg::BM && Cfg8::BN == Cfg::BN && Cfg8::BK == Cfg::BK &&
+                          Cfg8::B_BOX_N == Cfg::B_BOX_N,
+                      "same tensor-map boxes");
+        if (p.sk_units > 0)
+            launch_pdl(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_STREAM_K>, grid, Cfg::NUM_THREADS,
+                       Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
+        else if (p.num_tiles <= ctx->num_sms)   // one wave: eight epilogue warps
+            launch_pdl(gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_TILES>, grid, Cfg8::NUM_THREADS,
+                       Cfg8::SMEM_BYTES, stream, ta, tb, tc, p);
+        else
+            launch_pdl(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_TILES>, grid, Cfg::NUM_THREADS,
+                       Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -361,6 +372,9 @@ int gemm_create(gemm_ctx **out, int device)
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_STREAM_K>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_TILES>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg8::SMEM_BYTES);
     if (e != cudaSuccess) {
         delete ctx;
         return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);
@@ -387,14 +401,14 @@ int gemm_create(gemm_ctx **out, int device)
     // the non-portable cluster attribute; a size that cannot be scheduled stays 0 and the
     // widths it would serve are refused).
     {
-        auto *rk = gb300::gemm_tcgen05_kernel<SmCfg, gb300::SCHED_ROW_CLUSTER>;
-        if (cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize, SmCfg::SMEM_BYTES) == cudaSuccess &&
+        auto *rk = gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_ROW_CLUSTER>;
+        if (cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg8::SMEM_BYTES) == cudaSuccess &&
             cudaFuncSetAttribute(rk, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
             for (int cs = 1; cs <= kRowClusterMax; ++cs) {
                 cudaLaunchConfig_t lc = {};
                 lc.gridDim = dim3(static_cast<unsigned>(cs * (sms / cs)), 1, 1);
-                lc.blockDim = dim3(SmCfg::NUM_THREADS, 1, 1);
-                lc.dynamicSmemBytes = SmCfg::SMEM_BYTES;
+                lc.blockDim = dim3(Cfg8::NUM_THREADS, 1, 1);
+                lc.dynamicSmemBytes = Cfg8::SMEM_BYTES;
                 cudaLaunchAttribute a[1];
                 a[0].id = cudaLaunchAttributeClusterDimension;
                 a[0].val.clusterDim.x = static_cast<unsigned>(cs);
