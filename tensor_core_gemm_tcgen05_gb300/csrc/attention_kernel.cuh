@@ -18,9 +18,10 @@
 //  * warp 1: MMA issuer. S_t = Q_t K_j^T (M = N = 128, K = 128, both operands K-major from
 //    shared memory) into tile t's TMEM score columns; O_t += P_t V_j with P_t read from Tensor
 //    Memory (written by the softmax over the first half of the score columns, FP16 pairs)
-//    and V MN-major from shared memory. Issue order per key block j: P_A V_j, S_A for block
-//    j + 1, P_B V_j, S_B for block j + 1, so that the tensor cores work on one tile while
-//    the other tile's softmax runs;
+//    and V MN-major from shared memory, in two halves: keys 0..63 as soon as the softmax has
+//    written their P, keys 64..127 once all of P is written. Issue order per key block j:
+//    P_A V_j, S_A for block j + 1, P_B V_j, S_B for block j + 1, so that the tensor cores work
+//    on one tile while the other tile's softmax runs;
 //  * warps 2..5 (tile A) and 6..9 (tile B): online softmax, one query row per thread (its
 //    TMEM lane). Per block: the row maximum of the scores; when it exceeds the running
 //    maximum by more than kRescaleThreshold, the row of O is rescaled in TMEM (after the
@@ -61,8 +62,9 @@ struct AttnConfig {
     static constexpr int Q_OFF = 0;
     static constexpr int KV_OFF = TILES * TILE_BYTES;
     static constexpr int BAR_OFF = KV_OFF + KV_STAGES * 2 * TILE_BYTES;
-    // barriers: q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2], drain
-    static constexpr int NUM_BARS = 1 + 2 * KV_STAGES + 3 * TILES + 1;
+    // barriers: q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2], drain,
+    // p_half[2] (the first 64 keys' P written)
+    static constexpr int NUM_BARS = 1 + 2 * KV_STAGES + 4 * TILES + 1;
     static constexpr int SMEM_BYTES = 1024 + BAR_OFF + NUM_BARS * 8 + 16;
     static constexpr int NUM_THREADS = 64 + TILES * 128;
     // TMEM: S_A | S_B | O_A | O_B, 128 columns each; P_t over the first 64 columns of S_t
@@ -128,8 +130,8 @@ __device__ __forceinline__ void two_buffered_chunks(uint32_t addr, uint32_t (&va
 // columns that were already read), summing p into the running denominator l. At the end the
 // row of O is divided by l and stored.
 __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint32_t tmem, int tile, uint32_t s_full,
-                                                       uint32_t p_full, uint32_t pv_done, const WaitCtl &wc, int warp,
-                                                       int lane, int q0, int h, int n_kv)
+                                                       uint32_t p_half, uint32_t p_full, uint32_t pv_done,
+                                                       const WaitCtl &wc, int warp, int lane, int q0, int h, int n_kv)
 {
     using Cfg = AttnConfig;
     const int quarter = warp & 3;
@@ -238,7 +240,25 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
             }
             tmem_st_32x32b_x16(s_addr + 16u * static_cast<uint32_t>(c), pk);   // P over read scores
         };
-        two_buffered_chunks(s_addr, va, vb, p_chunk);
+        // P of keys 0..63 first, announced on p_half so that P V can start on them while keys
+        // 64..127 are computed
+        tmem_ld_32x32b_x32(s_addr, va);
+        tmem_ld_wait_regs(va);
+        tmem_ld_32x32b_x32(s_addr + 32u, vb);
+        p_chunk(va, 0);
+        tmem_ld_wait_regs(vb);
+        tmem_ld_32x32b_x32(s_addr + 64u, va);
+        p_chunk(vb, 1);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(p_half);
+        tmem_ld_wait_regs(va);
+        tmem_ld_32x32b_x32(s_addr + 96u, vb);
+        p_chunk(va, 2);
+        tmem_ld_wait_regs(vb);
+        p_chunk(vb, 3);
         float s0, s1;
         f32x2_unpack(f32x2_add(f32x2_add(sum2[0], sum2[1]), f32x2_add(sum2[2], sum2[3])), s0, s1);
         l = l * alpha + (s0 + s1);
@@ -296,6 +316,7 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
     const uint32_t kv_full0 = q_full + 8u, kv_empty0 = kv_full0 + 8u * Cfg::KV_STAGES;
     const uint32_t s_full0 = kv_empty0 + 8u * Cfg::KV_STAGES, p_full0 = s_full0 + 8u * Cfg::TILES;
     const uint32_t pv_done0 = p_full0 + 8u * Cfg::TILES, drain = pv_done0 + 8u * Cfg::TILES;
+    const uint32_t p_half0 = drain + 8u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sp + Cfg::BAR_OFF + Cfg::NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -319,6 +340,7 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
             mbar_init(s_full0 + 8u * t, 1);
             mbar_init(p_full0 + 8u * t, 4);   // the four softmax warps of tile t
             mbar_init(pv_done0 + 8u * t, 1);
+            mbar_init(p_half0 + 8u * t, 4);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -390,17 +412,21 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
                 umma_commit(s_full0 + 8u * t);
             };
             // O_t += P_t V_j, P_t from TMEM (8 columns per 16 keys)
+            // (keys 0..63 as soon as their P is written, keys 64..127 once all of it is)
             auto issue_pv = [&](int t, int j) -> bool {
-                if (!wait_bounded(p_full0 + 8u * t, static_cast<uint32_t>(j) & 1u, wc, ERR_MMA_OPERANDS))
-                    return false;
-                tc_fence_after_sync();
                 const uint32_t sV = sKV + static_cast<uint32_t>(j & 1) * 2u * TILE + TILE;
                 const uint32_t d = tmem + static_cast<uint32_t>(Cfg::O_COL + t * Cfg::D);
                 const uint32_t a = tmem + static_cast<uint32_t>(Cfg::S_COL + t * Cfg::BQ);
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t bar = (part == 0 ? p_half0 : p_full0) + 8u * t;
+                    if (!wait_bounded(bar, static_cast<uint32_t>(j) & 1u, wc, ERR_MMA_OPERANDS))
+                        return false;
+                    tc_fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < Cfg::BKV / 16; ++kk)
-                    umma_f16_tmem_a(d, a + 8u * static_cast<uint32_t>(kk), v_step_desc(sV, kk), ID_PV,
-                                    (j | kk) != 0 ? 1u : 0u);
+                    for (int kk = 4 * part; kk < 4 * part + 4; ++kk)
+                        umma_f16_tmem_a(d, a + 8u * static_cast<uint32_t>(kk), v_step_desc(sV, kk), ID_PV,
+                                        (j | kk) != 0 ? 1u : 0u);
+                }
                 umma_commit(pv_done0 + 8u * t);
                 return true;
             };
@@ -453,8 +479,8 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
     } else {
         // ---------------------------------------------------------------- online softmax
         const int t = (warp - 2) >> 2;   // warps 2..5: tile A, 6..9: tile B
-        attention_softmax_warp(p, tmem, t, s_full0 + 8u * t, p_full0 + 8u * t, pv_done0 + 8u * t, wc, warp, lane,
-                               q0 + t * Cfg::BQ, h, n_kv);
+        attention_softmax_warp(p, tmem, t, s_full0 + 8u * t, p_half0 + 8u * t, p_full0 + 8u * t, pv_done0 + 8u * t, wc,
+                               warp, lane, q0 + t * Cfg::BQ, h, n_kv);
     }
 
     tc_fence_before_sync();
