@@ -112,8 +112,8 @@ int gemm_run(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, cons
 /* The same operation on HOST buffers (pinned memory gives asynchronous copies; pageable
  * memory works but is copied synchronously). Device staging buffers, two internal copy
  * streams and their events are owned by the context (created or grown on first use, freed
- * by gemm_destroy). Outputs under 32 MiB are done in one piece; larger ones in up to 4
- * bands of whole 256-wide tiles whose uploads, GEMMs (one kernel launch each, on `stream`)
+ * by gemm_destroy). Outputs under 32 MiB are done in one piece; larger ones in 4 bands (8
+ * from 256 MiB on) of whole 256-wide tiles whose uploads, GEMMs (one kernel launch each, on `stream`)
  * and downloads overlap: column bands of C when A is the smaller operand (A goes first,
  * whole, then B in column bands), row bands otherwise (B whole, then A in row bands); the
  * softmax epilogue always uses row bands. Returns after C is on the host (the call
