@@ -237,6 +237,43 @@ def device_buffers(w, device):
 SOFTMAX_SHAPE = (8192, 16384)   # the MLP output's shape: 268 MB in, 268 MB out
 
 
+def measure_cublas_context(device, peaks, steps=20):
+    """Context only, not part of this library's path: cuBLAS (through torch.matmul) on the
+    plain FP16 problems, FP32 accumulation forced, same kind of timing (back-to-back launches
+    after warm-up, CUDA events)."""
+    import torch
+    from tensor_core_gemm_tcgen05_gb300 import inputs
+    prev = torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction
+    torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = False
+    out = {}
+    try:
+        for name in ("gemm_8192", "mlp_up_8200x4096x16384_none", "gemm_2048"):
+            w = inputs.WORKLOADS[name]
+            A = torch.randn(w.M, w.K, device=device).half()
+            B = torch.randn(w.K, w.N, device=device).half()
+            C = torch.empty(w.M, w.N, device=device, dtype=torch.float16)
+            n = steps if w.flops > 1e11 else 10 * steps
+            for _ in range(5):
+                torch.matmul(A, B, out=C)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                torch.matmul(A, B, out=C)
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) / n * 1e3
+            tf = w.flops / (us * 1e-6) / 1e12
+            out[f"cublas_context_{name}"] = {"tflops": round(tf, 2), "us_per_launch": round(us, 2),
+                                             "pct_of_burst_peak": round(100 * tf / float(peaks["bf16_tflops"]), 2)}
+            del A, B, C
+    finally:
+        torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = prev
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_softmax(g, ctx, stream, device, peaks, steps=50):
     """Row-wise softmax (the next hot-path row): HBM-bound, so GB/s against the measured copy
     bandwidth; algorithmic bytes = one read and one write of every FP16 element."""
@@ -464,6 +501,7 @@ def run_ours(args):
                           "pct_of_burst_peak": round(100 * tf / float(peaks["bf16_tflops"]), 2)}
             del a, b, bi, c
         torch.cuda.empty_cache()
+        side.update(measure_cublas_context(device, peaks))
         side.update(measure_softmax(g, ctx, stream, device, peaks))
         side.update(measure_fused_softmax(g, ctx, stream, device, peaks))
         side.update(measure_attention(g, ctx, stream, device, peaks))
