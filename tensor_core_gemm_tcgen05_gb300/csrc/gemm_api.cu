@@ -46,6 +46,7 @@ int raster_group(int m_blocks, int rows_per_block, int K)
     return static_cast<int>(std::max<int64_t>(kMinGroup, std::min<int64_t>(m_blocks, g)));
 }
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int64_t kSoftmaxMaxCtas = int64_t(1) << 20;   // row softmax grid cap (CTAs loop past it)
 constexpr int kSoftmaxTileN = 256;    // columns of C per CTA of a softmax row cluster
 constexpr int kRowClusterMax = 16;    // clusters of up to 16 CTAs (N <= 4096)
 // gemm_run_host splits M into at most this many chunks whose uploads, GEMMs and downloads
@@ -335,6 +336,18 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     if (e != cudaSuccess)
         return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
     return GEMM_OK;
+}
+
+// Row softmax with the rows in registers: G threads per row, V 16-byte vectors per thread,
+// register budget for MIN_CTAS CTAs per SM. One CTA per row group (the hardware balances
+// them); past kSoftmaxMaxCtas CTAs the kernel's CTAs loop over the remaining rows.
+template <int G, int V, int MIN_CTAS>
+void launch_softmax_regs(int64_t rows, int cols, const __half *x, __half *y, cudaStream_t st)
+{
+    constexpr int BLOCK = G < 256 ? 256 : G;
+    constexpr int GROUPS = BLOCK / G;
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>((rows + GROUPS - 1) / GROUPS, kSoftmaxMaxCtas));
+    gb300::row_softmax_regs_kernel<G, V, MIN_CTAS><<<grid, BLOCK, 0, st>>>(x, y, rows, cols);
 }
 
 }  // namespace
@@ -753,15 +766,28 @@ int gemm_row_softmax(gemm_ctx *ctx, int64_t rows, int64_t cols, const void *X, v
     DeviceGuard guard(ctx->device);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int c = static_cast<int>(cols);
-    // one warp per row up to 2048 columns (at most 8 vectors per lane), else a 256-thread block
-    if (cols <= 2048) {
-        const int64_t blocks = std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(ctx->num_sms) * 8);
-        gb300::row_softmax_kernel<32><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-            static_cast<const __half *>(X), static_cast<__half *>(Y), rows, c);
-    } else {
+    const __half *x = static_cast<const __half *>(X);
+    __half *y = static_cast<__half *>(Y);
+    // Rows held in registers (see launch_softmax_regs): a warp per row up to 2048 columns, a
+    // 256-thread CTA per row up to 16384. Longer rows are streamed twice (measured faster than
+    // 16 vectors per thread at one CTA per SM: the row's loads and arithmetic cannot overlap).
+    if (cols <= 256)
+        launch_softmax_regs<32, 1, 8>(rows, c, x, y, st);
+    else if (cols <= 512)
+        launch_softmax_regs<32, 2, 8>(rows, c, x, y, st);
+    else if (cols <= 1024)
+        launch_softmax_regs<32, 4, 4>(rows, c, x, y, st);
+    else if (cols <= 2048)
+        launch_softmax_regs<32, 8, 2>(rows, c, x, y, st);
+    else if (cols <= 4096)
+        launch_softmax_regs<256, 2, 8>(rows, c, x, y, st);
+    else if (cols <= 8192)
+        launch_softmax_regs<256, 4, 4>(rows, c, x, y, st);
+    else if (cols <= 16384)
+        launch_softmax_regs<256, 8, 2>(rows, c, x, y, st);
+    else {   // longer rows: streamed twice
         const int64_t blocks = std::min<int64_t>(rows, static_cast<int64_t>(ctx->num_sms) * 8);
-        gb300::row_softmax_kernel<256><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-            static_cast<const __half *>(X), static_cast<__half *>(Y), rows, c);
+        gb300::row_softmax_kernel<256><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, y, rows, c);
     }
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GEMM_OK : cuda_fail(ctx, e, GEMM_ERR_LAUNCH);

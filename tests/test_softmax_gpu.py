@@ -1,9 +1,9 @@
 """Parity of the row-wise softmax kernel (through the C ABI) with the FP64 oracle.
 
 Bound: every output within one FP16 ulp of the oracle's FP16 result (the GPU rounds an
-FP32 value, the oracle an FP64 one; exp2f and the FP32 sum add a few 1e-7 relative), with
-the ulp of the subnormal range (2^-24) for the smallest outputs. Guard bands around Y
-must stay untouched.
+FP32 value, the oracle an FP64 one; ex2.approx / exp2f and the FP32 sum add a few 1e-7
+relative), with the ulp of the subnormal range (2^-24) for the smallest outputs. Guard
+bands around Y must stay untouched.
 """
 import numpy as np
 import pytest
@@ -52,8 +52,13 @@ def run(ctx, X, inplace=False):
     return Y.cpu()
 
 
-@pytest.mark.parametrize("shape", [(1, 8), (3, 16), (1000, 264), (77, 2048), (64, 2056), (513, 16384),
-                                   (5, 65536), (2, 8), (300, 1000)],
+# Every dispatch path and its edges: rows in registers with a warp per row and 1/2/4/8
+# vectors per lane (up to 256, 512, 1024, 2048 columns) or a 256-thread CTA per row and
+# 2/4/8 vectors per thread (up to 4096, 8192, 16384), and the two-pass streaming kernel
+# beyond; full and ragged last vectors.
+@pytest.mark.parametrize("shape", [(1, 8), (3, 16), (1000, 264), (5, 520), (77, 2048), (64, 2056), (17, 6144),
+                                   (513, 16384), (33, 16392), (3, 24576), (9, 32768), (4, 32776), (5, 65536),
+                                   (2, 8), (300, 1000)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_row_softmax_matches_oracle(ctx, shape):
     rows, cols = shape
@@ -73,6 +78,19 @@ def test_row_softmax_textbook_row_padded_with_minus_inf(ctx):
     assert torch.allclose(Y[0, :3], torch.tensor([0.0900305732, 0.2447284711, 0.6652409558], dtype=torch.float64),
                           atol=3e-4, rtol=0)
     assert torch.all(Y[0, 3:] == 0) and torch.all(Y[1, :4] == 0.25) and torch.all(Y[1, 4:] == 0)
+
+
+@pytest.mark.parametrize("cols", [2048, 16384, 40000])
+def test_row_softmax_masked_prefix(ctx, cols):
+    """Rows whose leading columns are -inf (a masked prefix): the streamed kernel meets whole
+    steps of -inf before the first finite value; they must add nothing (no NaN)."""
+    X = inputs.random_fp16((3, cols), 91, scale=1.0) * 8
+    X[0, : cols - 16] = float("-inf")    # only the last 16 columns are finite
+    X[1, : cols // 2] = float("-inf")
+    Y = run(ctx, X)
+    ref, _ = oracle.softmax_rows(X)
+    assert_softmax_close(Y.numpy(), ref, f"masked prefix, {cols} columns")
+    assert torch.all(Y[0, : cols - 16] == 0) and torch.all(Y[1, : cols // 2] == 0)
 
 
 def test_row_softmax_in_place_and_large_values(ctx):
