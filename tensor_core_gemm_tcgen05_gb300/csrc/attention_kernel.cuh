@@ -30,6 +30,8 @@
 // Every mbarrier wait is bounded in time, as in the GEMM kernels.
 #pragma once
 
+#include <type_traits>
+
 #include "gemm_kernel.cuh"
 
 namespace gb300 {
@@ -152,122 +154,132 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
             return;
         tc_fence_after_sync();
         const int k0 = j * Cfg::BKV;
-        const bool full = k0 + Cfg::BKV - 1 <= kmax;   // no key of the block is masked for this row
-        // Block maximum of scale * s (base-2 units). On unmasked blocks: the maximum (minimum
-        // for a negative scale) of the raw scores in four independent three-input chains,
-        // scaled once.
-        float mb = -INFINITY;
-        float r0 = sl2 >= 0.0f ? -INFINITY : INFINITY, r1 = r0, r2 = r0, r3 = r0;
-        auto max_chunk = [&](const uint32_t(&x)[32], int c) {
-            if (full) {
-                if (sl2 >= 0.0f) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        r0 = fmax3(r0, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
-                        r1 = fmax3(r1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
-                        r2 = fmax3(r2, __uint_as_float(x[e + 4]), __uint_as_float(x[e + 5]));
-                        r3 = fmax3(r3, __uint_as_float(x[e + 6]), __uint_as_float(x[e + 7]));
+        // The block's work is compiled twice: without any masking when no key of the block is
+        // masked for any row of the warp (every block but the last, or the diagonal one when
+        // causal), and with the per-key mask otherwise. The choice is warp-uniform: the body
+        // holds warp-collective Tensor Memory loads and stores.
+        const bool all_full = __all_sync(0xffffffffu, k0 + Cfg::BKV - 1 <= kmax);
+        auto block = [&](auto full_tag) -> bool {
+            constexpr bool full = decltype(full_tag)::value;
+            // Block maximum of scale * s (base-2 units). On unmasked blocks: the maximum (minimum
+            // for a negative scale) of the raw scores in four independent three-input chains,
+            // scaled once.
+            float mb = -INFINITY;
+            float r0 = sl2 >= 0.0f ? -INFINITY : INFINITY, r1 = r0, r2 = r0, r3 = r0;
+            auto max_chunk = [&](const uint32_t(&x)[32], int c) {
+                if constexpr (full) {
+                    if (sl2 >= 0.0f) {
+    #pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            r0 = fmax3(r0, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+                            r1 = fmax3(r1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
+                            r2 = fmax3(r2, __uint_as_float(x[e + 4]), __uint_as_float(x[e + 5]));
+                            r3 = fmax3(r3, __uint_as_float(x[e + 6]), __uint_as_float(x[e + 7]));
+                        }
+                    } else {
+    #pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            r0 = fmin3(r0, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+                            r1 = fmin3(r1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
+                            r2 = fmin3(r2, __uint_as_float(x[e + 4]), __uint_as_float(x[e + 5]));
+                            r3 = fmin3(r3, __uint_as_float(x[e + 6]), __uint_as_float(x[e + 7]));
+                        }
                     }
                 } else {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        r0 = fmin3(r0, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
-                        r1 = fmin3(r1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
-                        r2 = fmin3(r2, __uint_as_float(x[e + 4]), __uint_as_float(x[e + 5]));
-                        r3 = fmin3(r3, __uint_as_float(x[e + 6]), __uint_as_float(x[e + 7]));
+    #pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (k0 + 32 * c + e <= kmax)
+                            mb = fmaxf(mb, __uint_as_float(x[e]) * sl2);
+                }
+            };
+            two_buffered_chunks(s_addr, va, vb, max_chunk);
+            if constexpr (full)
+                mb = (sl2 >= 0.0f ? fmax3(fmaxf(r0, r1), r2, r3) : fmin3(fminf(r0, r1), r2, r3)) * sl2;
+            // keep the old maximum unless this block's exceeds it by more than the threshold
+            const bool raise = mb > m + kRescaleThreshold || m == -INFINITY;
+            const float m_new = raise ? mb : m;
+            const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+            const float alpha = raise ? ex2_approx(m - m_use) : 1.0f;   // 0 on the first block (m = -inf)
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                // P_t V of block j - 1 is pv_done's completion number j - 1
+                if (lane == 0)
+                    w = wait_bounded(pv_done, static_cast<uint32_t>(j - 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, w, 0))
+                    return false;
+                tc_fence_after_sync();
+    #pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld_32x32b_x32(o_addr + 32u * c, v);
+                    tmem_ld_wait_regs(v);
+    #pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float a, b;
+                        f32x2_unpack(f32x2_mul(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                               f32x2_pack(alpha, alpha)),
+                                     a, b);
+                        v[e] = __float_as_uint(a);
+                        v[e + 1] = __float_as_uint(b);
                     }
+                    tmem_st_32x32b_x32(o_addr + 32u * c, v);
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if (k0 + 32 * c + e <= kmax)
-                        mb = fmaxf(mb, __uint_as_float(x[e]) * sl2);
+                tmem_st_wait();
             }
-        };
-        two_buffered_chunks(s_addr, va, vb, max_chunk);
-        if (full)
-            mb = (sl2 >= 0.0f ? fmax3(fmaxf(r0, r1), r2, r3) : fmin3(fminf(r0, r1), r2, r3)) * sl2;
-        // keep the old maximum unless this block's exceeds it by more than the threshold
-        const bool raise = mb > m + kRescaleThreshold || m == -INFINITY;
-        const float m_new = raise ? mb : m;
-        const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-        const float alpha = raise ? ex2_approx(m - m_use) : 1.0f;   // 0 on the first block (m = -inf)
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-            // P_t V of block j - 1 is pv_done's completion number j - 1
-            if (lane == 0)
-                w = wait_bounded(pv_done, static_cast<uint32_t>(j - 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
-            if (!__shfl_sync(0xffffffffu, w, 0))
-                return;
-            tc_fence_after_sync();
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld_32x32b_x32(o_addr + 32u * c, v);
-                tmem_ld_wait_regs(v);
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float a, b;
-                    f32x2_unpack(f32x2_mul(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
-                                           f32x2_pack(alpha, alpha)),
-                                 a, b);
-                    v[e] = __float_as_uint(a);
-                    v[e + 1] = __float_as_uint(b);
+            // four independent packed partial sums
+            uint64_t sum2[4] = {f32x2_pack(0.0f, 0.0f), f32x2_pack(0.0f, 0.0f), f32x2_pack(0.0f, 0.0f),
+                                f32x2_pack(0.0f, 0.0f)};
+            const uint64_t scale2 = f32x2_pack(sl2, sl2), neg_m2 = f32x2_pack(-m_use, -m_use);
+            auto p_chunk = [&](const uint32_t(&x)[32], int c) {
+                uint32_t pk[16];
+    #pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float t0, t1;
+                    f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])), scale2,
+                                           neg_m2),
+                                 t0, t1);
+                    float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+                    if constexpr (!full) {
+                        const int k = k0 + 32 * c + 2 * i;
+                        p0 = k <= kmax ? p0 : 0.0f;
+                        p1 = k + 1 <= kmax ? p1 : 0.0f;
+                    }
+                    sum2[i & 3] = f32x2_add(sum2[i & 3], f32x2_pack(p0, p1));
+                    __half2 hh = __floats2half2_rn(p0, p1);
+                    pk[i] = *reinterpret_cast<uint32_t *>(&hh);
                 }
-                tmem_st_32x32b_x32(o_addr + 32u * c, v);
-            }
+                tmem_st_32x32b_x16(s_addr + 16u * static_cast<uint32_t>(c), pk);   // P over read scores
+            };
+            // P of keys 0..63 first, announced on p_half so that P V can start on them while keys
+            // 64..127 are computed
+            tmem_ld_32x32b_x32(s_addr, va);
+            tmem_ld_wait_regs(va);
+            tmem_ld_32x32b_x32(s_addr + 32u, vb);
+            p_chunk(va, 0);
+            tmem_ld_wait_regs(vb);
+            tmem_ld_32x32b_x32(s_addr + 64u, va);
+            p_chunk(vb, 1);
             tmem_st_wait();
-        }
-        // four independent packed partial sums
-        uint64_t sum2[4] = {f32x2_pack(0.0f, 0.0f), f32x2_pack(0.0f, 0.0f), f32x2_pack(0.0f, 0.0f),
-                            f32x2_pack(0.0f, 0.0f)};
-        const uint64_t scale2 = f32x2_pack(sl2, sl2), neg_m2 = f32x2_pack(-m_use, -m_use);
-        auto p_chunk = [&](const uint32_t(&x)[32], int c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float t0, t1;
-                f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])), scale2,
-                                       neg_m2),
-                             t0, t1);
-                float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-                if (!full) {
-                    const int k = k0 + 32 * c + 2 * i;
-                    p0 = k <= kmax ? p0 : 0.0f;
-                    p1 = k + 1 <= kmax ? p1 : 0.0f;
-                }
-                sum2[i & 3] = f32x2_add(sum2[i & 3], f32x2_pack(p0, p1));
-                __half2 hh = __floats2half2_rn(p0, p1);
-                pk[i] = *reinterpret_cast<uint32_t *>(&hh);
-            }
-            tmem_st_32x32b_x16(s_addr + 16u * static_cast<uint32_t>(c), pk);   // P over read scores
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(p_half);
+            tmem_ld_wait_regs(va);
+            tmem_ld_32x32b_x32(s_addr + 96u, vb);
+            p_chunk(va, 2);
+            tmem_ld_wait_regs(vb);
+            p_chunk(vb, 3);
+            float s0, s1;
+            f32x2_unpack(f32x2_add(f32x2_add(sum2[0], sum2[1]), f32x2_add(sum2[2], sum2[3])), s0, s1);
+            l = l * alpha + (s0 + s1);
+            m = m_new;
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(p_full);   // P_t written (and O_t rescaled): the MMA warp may multiply
+            return true;
         };
-        // P of keys 0..63 first, announced on p_half so that P V can start on them while keys
-        // 64..127 are computed
-        tmem_ld_32x32b_x32(s_addr, va);
-        tmem_ld_wait_regs(va);
-        tmem_ld_32x32b_x32(s_addr + 32u, vb);
-        p_chunk(va, 0);
-        tmem_ld_wait_regs(vb);
-        tmem_ld_32x32b_x32(s_addr + 64u, va);
-        p_chunk(vb, 1);
-        tmem_st_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(p_half);
-        tmem_ld_wait_regs(va);
-        tmem_ld_32x32b_x32(s_addr + 96u, vb);
-        p_chunk(va, 2);
-        tmem_ld_wait_regs(vb);
-        p_chunk(vb, 3);
-        float s0, s1;
-        f32x2_unpack(f32x2_add(f32x2_add(sum2[0], sum2[1]), f32x2_add(sum2[2], sum2[3])), s0, s1);
-        l = l * alpha + (s0 + s1);
-        m = m_new;
-        tmem_st_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(p_full);   // P_t written (and O_t rescaled): the MMA warp may multiply
+        if (!(all_full ? block(std::true_type{}) : block(std::false_type{})))
+            return;
     }
     if (n_kv == 0)
         return;
