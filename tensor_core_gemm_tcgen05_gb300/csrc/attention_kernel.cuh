@@ -145,7 +145,7 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
     const int kmax = p.causal ? min(p.Sk - 1, qi) : p.Sk - 1;   // last key this row sees
     const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.0f;
-    uint32_t v[32], va[32], vb[32];
+    uint32_t va[32], vb[32];
     for (int j = 0; j < n_kv; ++j) {
         int w = 1;
         if (lane == 0)
@@ -209,18 +209,18 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
                 tc_fence_after_sync();
     #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
-                    tmem_ld_32x32b_x32(o_addr + 32u * c, v);
-                    tmem_ld_wait_regs(v);
+                    tmem_ld_32x32b_x32(o_addr + 32u * c, va);
+                    tmem_ld_wait_regs(va);
     #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float a, b;
-                        f32x2_unpack(f32x2_mul(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                        f32x2_unpack(f32x2_mul(f32x2_pack(__uint_as_float(va[e]), __uint_as_float(va[e + 1])),
                                                f32x2_pack(alpha, alpha)),
                                      a, b);
-                        v[e] = __float_as_uint(a);
-                        v[e + 1] = __float_as_uint(b);
+                        va[e] = __float_as_uint(a);
+                        va[e + 1] = __float_as_uint(b);
                     }
-                    tmem_st_32x32b_x32(o_addr + 32u * c, v);
+                    tmem_st_32x32b_x32(o_addr + 32u * c, va);
                 }
                 tmem_st_wait();
             }
@@ -293,16 +293,16 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
     __half *orow = p.O + (static_cast<int64_t>(h) * p.Sq + qi) * Cfg::D;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
-        tmem_ld_32x32b_x32(o_addr + 32u * c, v);
-        tmem_ld_wait_regs(v);
+        tmem_ld_32x32b_x32(o_addr + 32u * c, va);
+        tmem_ld_wait_regs(va);
         if (qi < p.Sq) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    __half2 hh = __floats2half2_rn(__uint_as_float(v[8 * i + 2 * e]) * inv,
-                                                   __uint_as_float(v[8 * i + 2 * e + 1]) * inv);
+                    __half2 hh = __floats2half2_rn(__uint_as_float(va[8 * i + 2 * e]) * inv,
+                                                   __uint_as_float(va[8 * i + 2 * e + 1]) * inv);
                     pk[e] = *reinterpret_cast<uint32_t *>(&hh);
                 }
                 *reinterpret_cast<uint4 *>(orow + 32 * c + 8 * i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
