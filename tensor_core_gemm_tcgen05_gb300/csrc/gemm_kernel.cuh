@@ -577,17 +577,37 @@ __device__ __forceinline__ void softmax_pass1(const GemmParams &p, uint32_t tadd
                 if (n0 + j >= p.N)
                     v[j] = -INFINITY;   // not a column of C: contributes 2^-inf = 0
         }
-        float cm = v[0];
+        // chunk maximum in four independent three-input chains
+        float q0 = fmax3(v[0], v[1], v[2]), q1 = fmax3(v[3], v[4], v[5]);
+        float q2 = fmax3(v[6], v[7], v[8]), q3 = fmax3(v[9], v[10], v[11]);
 #pragma unroll
-        for (int j = 1; j < 32; ++j)
-            cm = fmaxf(cm, v[j]);
-        float cs = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float e = ex2_approx(v[j] - cm);
-            cs += e;
-            r[j] = __float_as_uint(e);
+        for (int j = 12; j < 28; j += 8) {
+            q0 = fmax3(q0, v[j], v[j + 1]);
+            q1 = fmax3(q1, v[j + 2], v[j + 3]);
+            q2 = fmax3(q2, v[j + 4], v[j + 5]);
+            q3 = fmax3(q3, v[j + 6], v[j + 7]);
         }
+        q0 = fmax3(q0, v[28], v[29]);
+        q1 = fmax3(q1, v[30], v[31]);
+        const float cm = fmax3(fmaxf(q0, q1), q2, q3);
+        // 2^(v - cm), summed in two packed partial sums
+        const uint64_t neg_cm = f32x2_pack(-cm, -cm);
+        uint64_t sa = f32x2_pack(0.0f, 0.0f), sb = sa;
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            float d0, d1;
+            f32x2_unpack(f32x2_add(f32x2_pack(v[j], v[j + 1]), neg_cm), d0, d1);
+            const float e0 = ex2_approx(d0), e1 = ex2_approx(d1);
+            if ((j & 2) == 0)
+                sa = f32x2_add(sa, f32x2_pack(e0, e1));
+            else
+                sb = f32x2_add(sb, f32x2_pack(e0, e1));
+            r[j] = __float_as_uint(e0);
+            r[j + 1] = __float_as_uint(e1);
+        }
+        float s0, s1;
+        f32x2_unpack(f32x2_add(sa, sb), s0, s1);
+        const float cs = s0 + s1;
         tmem_st_32x32b_x32(taddr + 32u * c, r);
         mc[c] = cm;
         merge_stats(m, s, cm, cs);
