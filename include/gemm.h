@@ -98,12 +98,16 @@ int gemm_create(gemm_ctx **out, int device);
  * Ownership: the caller owns every buffer and must keep them alive until the stream has
  * passed this call. gemm_run allocates nothing and launches exactly one kernel.
  * Schedule: 256 x 256 tiles on CTA pairs when there are at least as many as co-resident
- * pairs; otherwise 128 x 256 tiles on single SMs, and when those are at most half the SMs
- * and K gives at least twice as many CTAs as tiles 16 k-blocks of 64 each, stream-K: the
- * tiles' k-blocks are split evenly over up to every SM, and a tile cut between SMs is
- * summed in FP32 through the context's workspace before its epilogue (so the summation
- * order, not the result's tolerance, differs from the whole-tile schedule). Never for
- * GEMM_EPI_SOFTMAX.
+ * pairs; otherwise 128 x 256 tiles on single SMs. When those tiles leave most SMs idle:
+ * split-K, a cluster of S = 8, 4 or 2 CTAs per tile (the largest S with tiles x S <= SMs,
+ * all clusters co-resident, and at least 8 k-blocks of 64 per CTA), each CTA summing 1/S of
+ * the k-blocks; the S FP32 partials are added over distributed shared memory in a fixed
+ * order and the CTA of rank r applies the epilogue to rows [r*128/S, (r+1)*128/S) of the
+ * tile. Failing that, when the tiles are at most half the SMs and K gives at least twice as
+ * many CTAs as tiles 16 k-blocks each, stream-K: the tiles' k-blocks are split evenly over
+ * up to every SM, and a tile cut between SMs is summed in FP32 through the context's
+ * workspace before its epilogue. (Both change the summation order, not the result's
+ * tolerance, against the whole-tile schedule.) Never for GEMM_EPI_SOFTMAX.
  * Errors: see gemm_status. A wait that runs out inside the kernel is reported later by
  * gemm_last_device_error, not by this call. */
 int gemm_run(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, const void *B,
@@ -197,13 +201,18 @@ int gemm_attention_fwd(gemm_ctx *ctx, int64_t heads, int64_t seq_q, int64_t seq_
  *       pair kernel cannot run);
  *     GEMM_DEBUG_FORCE_STREAMK: the one-CTA kernel always takes the stream-K schedule,
  *       with one CTA per k-block unit up to one per SM (so that tiles are cut into many
- *       parts), except for GEMM_EPI_SOFTMAX. */
+ *       parts), except for GEMM_EPI_SOFTMAX;
+ *     GEMM_DEBUG_FORCE_SPLITK: the one-CTA kernel (never the pair kernel) takes the
+ *       split-K schedule whenever K has at least 2 k-blocks, with the largest S of 8, 4, 2
+ *       not above the k-blocks, for any number of tiles (clusters then run in several
+ *       waves), except for GEMM_EPI_SOFTMAX; FORCE_STREAMK takes precedence. */
 enum {
     GEMM_DEBUG_NONE = 0,
     GEMM_DEBUG_WITHHOLD_FIRST_LOAD = 1,
     GEMM_DEBUG_FORCE_SINGLE = 2,
     GEMM_DEBUG_FORCE_PAIR = 4,
-    GEMM_DEBUG_FORCE_STREAMK = 8
+    GEMM_DEBUG_FORCE_STREAMK = 8,
+    GEMM_DEBUG_FORCE_SPLITK = 16
 };
 int gemm_set_timeout_ns(gemm_ctx *ctx, uint64_t ns);
 int gemm_set_debug(gemm_ctx *ctx, int flags);

@@ -37,6 +37,7 @@ GEMM_DEBUG_WITHHOLD_FIRST_LOAD = 1
 GEMM_DEBUG_FORCE_SINGLE = 2
 GEMM_DEBUG_FORCE_PAIR = 4
 GEMM_DEBUG_FORCE_STREAMK = 8
+GEMM_DEBUG_FORCE_SPLITK = 16
 
 # Every symbol include/gemm.h declares (the CPU tests check the library exports them).
 EXPORTS = (

@@ -61,6 +61,7 @@ constexpr uint64_t kMinTimeoutNs = 1000000ull;
 // 128 x 256 x 8192 (39.8 -> 28.0 us) but not for 128 tiles on 152 SMs (2048^3: 15.3 us
 // whole tiles, 23 us stream-K).
 constexpr int64_t kStreamKMinUnits = 16;
+constexpr int kSplitKMinBlocks = 8;   // split-K: k-blocks per CTA at least
 constexpr int kStreamKMinSpread = 2;
 
 }  // namespace
@@ -81,6 +82,8 @@ struct gemm_ctx {
     // softmax epilogue: co-resident clusters of cs CTAs (one per 256 columns), per cs
     // (0: that cluster size cannot be scheduled)
     int row_clusters[kRowClusterMax + 1] = {};
+    // split-K: co-resident clusters of 2, 4 and 8 CTAs of the split-K instance, per size
+    int split_clusters[9] = {};
     // gemm_run_host: device staging buffers, two copy streams and the events that order
     // the chunked pipeline (created on first use)
     void *stage = nullptr;
@@ -262,6 +265,7 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     p.epilogue = epilogue;
     p.bias = static_cast<const __half *>(bias);
     p.C = static_cast<__half *>(C);
+    p.ldc = ldc > 0 ? ldc : N;
     p.err = ctx->d_err;
     p.timeout_ns = ctx->timeout_ns;
     p.debug = ctx->debug & GEMM_DEBUG_WITHHOLD_FIRST_LOAD;
@@ -285,7 +289,7 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     }
     const int pair_tiles = ((M + PairCfg::BM - 1) / PairCfg::BM) * ((N + PairCfg::BN - 1) / PairCfg::BN);
     bool pair = ctx->max_clusters > 0 && pair_tiles >= ctx->max_clusters;
-    if (ctx->debug & GEMM_DEBUG_FORCE_SINGLE)
+    if (ctx->debug & (GEMM_DEBUG_FORCE_SINGLE | GEMM_DEBUG_FORCE_SPLITK))
         pair = false;
     if ((ctx->debug & GEMM_DEBUG_FORCE_PAIR) && ctx->max_clusters > 0)
         pair = true;
@@ -303,9 +307,32 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
         p.num_tiles = p.m_blocks * p.n_blocks;
         p.group_m = raster_group(p.m_blocks, Cfg::BM, K);
         int grid = std::min(p.num_tiles, ctx->num_sms);
-        // Stream-K when the tiles leave most SMs idle: the (tile, k-block) units are split
-        // evenly over up to every SM (the fused softmax needs whole rows in one CTA: never).
+        // Split-K when the tiles leave most SMs idle: a cluster of S CTAs per tile, each with
+        // 1/S of the k-blocks (at least kSplitKMinBlocks of them), the partials summed over
+        // DSMEM; S = 8, 4 or 2, the largest whose clusters all run at once. (The fused softmax
+        // needs whole rows in one CTA: never.)
         const int64_t units = static_cast<int64_t>(p.num_tiles) * p.num_kb;
+        int split = 0;
+        if (epilogue != GEMM_EPI_SOFTMAX && units > 0 && !(ctx->debug & GEMM_DEBUG_FORCE_STREAMK)) {
+            for (int cs = 8; cs >= 2 && !split; cs /= 2) {
+                if (ctx->split_clusters[cs] <= 0 || p.num_kb < cs)
+                    continue;
+                if (ctx->debug & GEMM_DEBUG_FORCE_SPLITK)
+                    split = cs;   // any tile count (several waves) and any k-blocks >= cs
+                else if (static_cast<int64_t>(p.num_tiles) * cs <= ctx->num_sms &&
+                         p.num_tiles <= ctx->split_clusters[cs] && p.num_kb >= kSplitKMinBlocks * cs)
+                    split = cs;
+            }
+        }
+        if (split > 0) {
+            p.split = split;
+            launch_pdl_cluster(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_SPLIT_K>, p.num_tiles * split, split,
+                               Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
+            const cudaError_t e = cudaGetLastError();
+            return e == cudaSuccess ? GEMM_OK : cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+        }
+        // Otherwise stream-K when the tiles leave most SMs idle: the (tile, k-block) units are
+        // split evenly over up to every SM.
         if (epilogue != GEMM_EPI_SOFTMAX && units > 0) {
             int g_sk = 0;
             if (ctx->debug & GEMM_DEBUG_FORCE_STREAMK)
@@ -410,6 +437,30 @@ int gemm_create(gemm_ctx **out, int device)
             ctx->max_clusters = clusters;
     }
     cudaGetLastError();
+    // Split-K clusters: how many clusters of 2, 4 and 8 CTAs fit at once (0: that size is not
+    // used).
+    {
+        auto *sk = gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_SPLIT_K>;
+        if (cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) == cudaSuccess) {
+            for (int cs = 2; cs <= 8; cs *= 2) {
+                cudaLaunchConfig_t lc = {};
+                lc.gridDim = dim3(static_cast<unsigned>(cs * (sms / cs)), 1, 1);
+                lc.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
+                lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+                cudaLaunchAttribute a[1];
+                a[0].id = cudaLaunchAttributeClusterDimension;
+                a[0].val.clusterDim.x = static_cast<unsigned>(cs);
+                a[0].val.clusterDim.y = 1;
+                a[0].val.clusterDim.z = 1;
+                lc.attrs = a;
+                lc.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, sk, &lc) == cudaSuccess)
+                    ctx->split_clusters[cs] = n;
+            }
+        }
+        cudaGetLastError();
+    }
     // Softmax row clusters: how many clusters of each size fit at once (sizes above 8 need
     // the non-portable cluster attribute; a size that cannot be scheduled stays 0 and the
     // widths it would serve are refused).
@@ -804,7 +855,7 @@ int gemm_set_timeout_ns(gemm_ctx *ctx, uint64_t ns)
 int gemm_set_debug(gemm_ctx *ctx, int flags)
 {
     if (!ctx || (flags & ~(GEMM_DEBUG_WITHHOLD_FIRST_LOAD | GEMM_DEBUG_FORCE_SINGLE | GEMM_DEBUG_FORCE_PAIR |
-                           GEMM_DEBUG_FORCE_STREAMK)))
+                           GEMM_DEBUG_FORCE_STREAMK | GEMM_DEBUG_FORCE_SPLITK)))
         return GEMM_ERR_ARG;
     ctx->debug = flags;
     return GEMM_OK;

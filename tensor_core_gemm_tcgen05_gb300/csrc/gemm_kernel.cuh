@@ -69,6 +69,7 @@ enum : int {
     SCHED_TILES = 0,         // whole tiles, grouped raster, persistent
     SCHED_STREAM_K = 1,      // equal ranges of (tile, k-block) units
     SCHED_ROW_CLUSTER = 2,   // one cluster per 128-row block, CTA r = column tile r
+    SCHED_SPLIT_K = 3,       // one cluster per tile, CTA r = the r-th of `split` equal k ranges
 };
 
 enum : int { EPI_NONE = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_SOFTMAX = 3 };
@@ -95,6 +96,8 @@ struct GemmParams {
     float *sk_ws = nullptr;          // [gridDim.x][epilogue warp][chunk][8][32 lanes][4] FP32 partials
     uint32_t *sk_flags = nullptr;    // [gridDim.x][epilogue warps]: 1 = that part is written
     int row_cluster = 0;             // row clusters: CTAs per cluster (= n_blocks)
+    int split = 0;                   // split-K: CTAs per cluster, each with 1/split of the k-blocks
+    int64_t ldc = 0;                 // row stride of C in elements (split-K writes C directly)
 };
 
 template <int BM_, int BN_, int STAGES_, int EPI_WARPS_ = 4>
@@ -189,6 +192,8 @@ __device__ __forceinline__ int64_t sk_begin(const GemmParams &p, int g)
 //  SCHED_STREAM_K: the pieces of the tiles that the CTA's unit range covers, in order.
 //  SCHED_ROW_CLUSTER: row blocks clusterid, clusterid + clusters, ...; column tile = the
 //  CTA's rank in its cluster.
+//  SCHED_SPLIT_K: tile clusterid; k-blocks [r * num_kb / split, (r + 1) * num_kb / split) for
+//  the CTA of rank r (never empty when num_kb >= split).
 template <int SCHED>
 struct WorkIter {
     int64_t u = 0, end = 0;
@@ -201,6 +206,9 @@ struct WorkIter {
         } else if constexpr (SCHED == SCHED_ROW_CLUSTER) {
             t = static_cast<int>(cluster_id_x());
             step = static_cast<int>(cluster_count_x());
+            rank = static_cast<int>(cluster_ctarank());
+        } else if constexpr (SCHED == SCHED_SPLIT_K) {
+            t = static_cast<int>(cluster_id_x());
             rank = static_cast<int>(cluster_ctarank());
         } else {
             t = static_cast<int>(blockIdx.x);
@@ -217,6 +225,15 @@ struct WorkIter {
             k1 = static_cast<int>(min(static_cast<int64_t>(p.num_kb), k0 + (end - u)));
             u += k1 - k0;
             tile_coords(p, tile, mb, nb);
+            return true;
+        } else if constexpr (SCHED == SCHED_SPLIT_K) {
+            if (u != 0 || t >= p.num_tiles)
+                return false;
+            u = 1;   // one segment
+            tile = t;
+            tile_coords(p, tile, mb, nb);
+            k0 = static_cast<int>(static_cast<int64_t>(rank) * p.num_kb / p.split);
+            k1 = static_cast<int>(static_cast<int64_t>(rank + 1) * p.num_kb / p.split);
             return true;
         } else if constexpr (SCHED == SCHED_ROW_CLUSTER) {
             if (t >= p.m_blocks)
@@ -844,6 +861,128 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t tadd
     }
 }
 
+// Split-K, step 1: an epilogue warp copies its 32 accumulator rows (all BN columns) into the
+// CTA's staging area (the idle operand ring): FP32 row r at r * BN * 4 bytes, its 16-byte
+// unit u stored at unit u ^ (r & 7), so that the eight lanes of a quarter-warp, eight
+// consecutive rows, write eight different bank groups.
+template <int BN>
+__device__ __forceinline__ void splitk_stage(uint32_t taddr, uint32_t stage_base, int row, int lane)
+{
+    (void)lane;
+    const uint32_t row_addr = stage_base + static_cast<uint32_t>(row) * (BN * 4);
+    const uint32_t sw = static_cast<uint32_t>(row & 7);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + 32u * static_cast<uint32_t>(c), v);
+        tmem_ld_wait_regs(v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(row_addr + (((static_cast<uint32_t>(8 * c + j)) ^ sw) << 4),
+                         make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+    }
+}
+
+// Split-K, step 2 (after a cluster barrier: every CTA's partial is staged): the CTA of rank
+// `rank` owns rows [rank * R, rank * R + R) of the tile, R = BM / S; epilogue warp w takes R / 4
+// of them, and lane l the 16-byte units l and l + 32 (columns 4l..4l+3 and 128+4l..) of each:
+// every load instruction of the warp reads 512 contiguous bytes of one staged row (of this
+// CTA's or another's, over DSMEM), and every store writes 256 contiguous bytes of C. Rows go
+// in four batches of 8 / S each (all S partials of a batch in flight, the next batch's loads
+// issued before the current one is added); the S partials are added in rank order, so the
+// result does not depend on timing. Then bias, activation, FP16 (rows past M and columns past
+// N are skipped; N is a multiple of 8, so a unit is either inside C or past it).
+template <int BM, int BN, int S>
+__device__ __forceinline__ void splitk_reduce_s(const GemmParams &p, uint32_t stage_base, int mb, int nb, int rank,
+                                                int tid)
+{
+    static_assert(BN == 256 && BM == 128, "two 16-byte units per lane per row");
+    constexpr int R = BM / S;
+    constexpr int ROWS_W = R / 4;                 // rows per warp
+    constexpr int ROWS_B = 8 / S;                 // rows per batch (16 loads per lane)
+    constexpr int BATCHES = ROWS_W / ROWS_B;      // 4
+    const int w = tid >> 5, lane = tid & 31;
+    const int r0 = rank * R + w * ROWS_W;         // first tile row of this warp
+    uint32_t src[S];
+#pragma unroll
+    for (int q = 0; q < S; ++q)
+        src[q] = mapa_shared(stage_base, static_cast<uint32_t>(q));
+    float4 buf[2][ROWS_B][2][S];
+    auto load = [&](int b, float4(&dst)[ROWS_B][2][S]) {
+#pragma unroll
+        for (int i = 0; i < ROWS_B; ++i) {
+            const int r = r0 + b * ROWS_B + i;
+            const uint32_t row_off = static_cast<uint32_t>(r) * (BN * 4);
+            const uint32_t sw = static_cast<uint32_t>(r & 7);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint32_t u = static_cast<uint32_t>(k * 32 + lane);
+#pragma unroll
+                for (int q = 0; q < S; ++q)
+                    dst[i][k][q] = ld_shared_cluster_f4(src[q] + row_off + ((u ^ sw) << 4));
+            }
+        }
+    };
+    load(0, buf[0]);
+#pragma unroll
+    for (int b = 0; b < BATCHES; ++b) {
+        if (b + 1 < BATCHES)
+            load(b + 1, buf[(b + 1) & 1]);
+        const float4(&cur)[ROWS_B][2][S] = buf[b & 1];
+#pragma unroll
+        for (int i = 0; i < ROWS_B; ++i) {
+            const int row = mb * BM + r0 + b * ROWS_B + i;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                float4 a = cur[i][k][0];
+#pragma unroll
+                for (int q = 1; q < S; ++q) {
+                    a.x += cur[i][k][q].x;
+                    a.y += cur[i][k][q].y;
+                    a.z += cur[i][k][q].z;
+                    a.w += cur[i][k][q].w;
+                }
+                const int col = nb * BN + 4 * (k * 32 + lane);
+                if (row >= p.M || col >= p.N)
+                    continue;
+                float v[4] = {a.x, a.y, a.z, a.w};
+                if (p.bias != nullptr) {
+                    const uint2 bv = __ldg(reinterpret_cast<const uint2 *>(p.bias + col));
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&bv.x));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&bv.y));
+                    v[0] += f0.x;
+                    v[1] += f0.y;
+                    v[2] += f1.x;
+                    v[3] += f1.y;
+                }
+                if (p.epilogue == EPI_GELU) {
+                    gelu_pair(v[0], v[1]);
+                    gelu_pair(v[2], v[3]);
+                } else if (p.epilogue == EPI_RELU) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        v[e] = fmaxf(v[e], 0.0f);
+                }
+                __half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2], v[3]);
+                *reinterpret_cast<uint2 *>(p.C + static_cast<int64_t>(row) * p.ldc + col) =
+                    make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
+            }
+        }
+    }
+}
+
+template <int BM, int BN>
+__device__ __forceinline__ void splitk_reduce(const GemmParams &p, uint32_t stage_base, int mb, int nb, int rank,
+                                              int tid)
+{
+    if (p.split == 8)
+        splitk_reduce_s<BM, BN, 8>(p, stage_base, mb, nb, rank, tid);
+    else if (p.split == 4)
+        splitk_reduce_s<BM, BN, 4>(p, stage_base, mb, nb, rank, tid);
+    else
+        splitk_reduce_s<BM, BN, 2>(p, stage_base, mb, nb, rank, tid);
+}
+
 // SCHED: SCHED_TILES (whole tiles per CTA), SCHED_STREAM_K (p.sk_units > 0, workspace and
 // flags set) or SCHED_ROW_CLUSTER (launched in clusters of p.row_cluster = n_blocks CTAs,
 // softmax epilogue only).
@@ -1032,7 +1171,23 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         constexpr int64_t SLOT = static_cast<int64_t>(BM) * BN;
         const int64_t my_share = static_cast<int64_t>(ew) * (Cfg::PART_WARP_BYTES / 4);
         uint32_t part_phase = 0;
-        if constexpr (SCHED == SCHED_ROW_CLUSTER) {
+        if constexpr (SCHED == SCHED_SPLIT_K) {
+            // this CTA's partial sum of its tile into the staging area; the cluster reduces
+            // the partials after the barrier below
+            static_assert(Cfg::EPI_COL_GROUPS == 1 && BM * BN * 4 <= Cfg::STAGES * Cfg::STAGE_BYTES,
+                          "one warp per lane quarter; the staged partial fits the operand ring");
+            WorkIter<SCHED> work(p);
+            int t, mb, nb, k0, k1;
+            if (work.next(p, t, mb, nb, k0, k1)) {
+                int ok = 1;
+                if (lane == 0)
+                    ok = wait_bounded(accf0, 0u, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
+                if (__shfl_sync(0xffffffffu, ok, 0)) {
+                    tc_fence_after_sync();
+                    splitk_stage<BN>(tmem_base + lane_base, sA, quarter * 32 + lane, lane);
+                }
+            }
+        } else if constexpr (SCHED == SCHED_ROW_CLUSTER) {
             // Softmax over a row cluster, pipelined by one tile: pass 1 and the publication of
             // tile i's row statistics come before the collection and pass 2 of tile i - 1, so
             // that waiting for the other CTAs overlaps work (both TMEM accumulators hold a tile).
@@ -1191,6 +1346,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         __syncwarp();
     }
 
+    if constexpr (SCHED == SCHED_SPLIT_K) {
+        // every thread of every CTA of the cluster, on every path (also after a timeout)
+        cluster_sync();   // all partials are staged
+        if (warp >= 2) {
+            WorkIter<SCHED> work(p);
+            int t, mb, nb, k0, k1;
+            if (work.next(p, t, mb, nb, k0, k1) && *abort_flag == 0)
+                splitk_reduce<BM, BN>(p, sA, mb, nb, static_cast<int>(cluster_ctarank()),
+                                      static_cast<int>(threadIdx.x) - 64);
+        }
+        cluster_sync();   // no CTA leaves while another may still read its partial
+    }
     tc_fence_before_sync();
     __syncthreads();
     if constexpr (SCHED == SCHED_ROW_CLUSTER)

@@ -33,15 +33,18 @@ FORCE = {
     "single": g.GEMM_DEBUG_FORCE_SINGLE,
     "pair": g.GEMM_DEBUG_FORCE_PAIR,
     "streamk": g.GEMM_DEBUG_FORCE_SINGLE | g.GEMM_DEBUG_FORCE_STREAMK,
+    "splitk": g.GEMM_DEBUG_FORCE_SPLITK,
 }
 
 
 @pytest.fixture(params=list(FORCE))
 def kctx(ctx, request):
     """The context with the kernel choice forced: one-CTA 128x256 tiles, CTA-pair 256x256
-    tiles (cta_group::2), or one-CTA tiles under stream-K with one k-block unit per CTA (up
-    to one CTA per SM), so that most tiles are cut into several parts summed through the
-    workspace."""
+    tiles (cta_group::2), one-CTA tiles under stream-K with one k-block unit per CTA (up to
+    one CTA per SM), so that most tiles are cut into several parts summed through the
+    workspace, or one-CTA tiles under split-K (a cluster of 8, 4 or 2 CTAs per tile, the
+    largest not above the k-blocks, partials summed over distributed shared memory; K under
+    two k-blocks keeps whole tiles)."""
     if request.param == "pair" and g.gemm_num_pairs(ctx) == 0:
         pytest.skip("the pair kernel cannot run on this device")
     g.gemm_set_debug(ctx, FORCE[request.param])
@@ -396,6 +399,72 @@ def test_streamk_timeout_then_recovery(ctx):
         g.gemm_set_timeout_ns(ctx, 2_000_000_000)
 
 
+def test_splitk_timeout_then_recovery(ctx):
+    """Split-K in clusters of 8 with every CTA withholding its first load: every wait runs
+    out, every CTA still reaches both cluster barriers (no hang), the timeout is reported,
+    and the next split-K GEMM on the same context is correct."""
+    g.gemm_set_timeout_ns(ctx, 20_000_000)
+    g.gemm_set_debug(ctx, g.GEMM_DEBUG_WITHHOLD_FIRST_LOAD | FORCE["splitk"])
+    try:
+        dev = torch.device("cuda:0")
+        A = torch.ones(256, 1024, dtype=torch.float16, device=dev)
+        B = torch.ones(1024, 256, dtype=torch.float16, device=dev)
+        C = torch.zeros(256, 256, dtype=torch.float16, device=dev)
+        g.gemm(ctx, A, B, None, g.EPI_NONE, out=C)
+        torch.cuda.synchronize()
+        status, detail = g.gemm_last_device_error(ctx)
+        assert status == g.GEMM_ERR_TIMEOUT and detail in (1, 2, 3, 4, 5)
+        assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+        g.gemm_set_debug(ctx, FORCE["splitk"])
+        check(ctx, 256, 256, 1024, epi=g.EPI_GELU, with_bias=True, seed=13)
+    finally:
+        g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
+        g.gemm_set_timeout_ns(ctx, 2_000_000_000)
+
+
+@pytest.mark.parametrize("shape", [(128, 256, 1024), (200, 264, 520), (1000, 520, 8200), (384, 512, 192)],
+                         ids=lambda v: "x".join(map(str, v)))
+def test_splitk_cluster_sizes_and_tails(ctx, shape):
+    """Split-K with 8, 4 and 2 CTAs per tile (K = 1024, 520, 8200 and 192 give 16, 9, 129 and
+    3 k-blocks: uneven ranges, a ragged last k-block), rows and columns past M and N in the
+    last tiles, every epilogue; bit-identical between two runs (fixed summation order)."""
+    M, N, K = shape
+    g.gemm_set_debug(ctx, FORCE["splitk"])
+    try:
+        for epi, with_bias in ((g.EPI_NONE, False), (g.EPI_GELU, True), (g.EPI_RELU, True)):
+            check(ctx, M, N, K, epi=epi, with_bias=with_bias, seed=M + K + epi)
+        dev = torch.device("cuda:0")
+        A = inputs.random_fp16((M, K), 7).to(dev)
+        B = inputs.random_fp16((K, N), 8).to(dev)
+        C1 = torch.empty(M, N, dtype=torch.float16, device=dev)
+        C2 = torch.empty(M, N, dtype=torch.float16, device=dev)
+        g.gemm(ctx, A, B, None, g.EPI_NONE, out=C1)
+        g.gemm(ctx, A, B, None, g.EPI_NONE, out=C2)
+        torch.cuda.synchronize()
+        assert torch.equal(C1, C2)
+        assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+    finally:
+        g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
+
+
+def test_splitk_in_host_column_bands(ctx):
+    """Split-K inside gemm_run_host's column bands: each band's C is a slice of a wider
+    matrix (row stride N, not the band's width), which split-K writes directly."""
+    M, N, K = 2056, 8200, 512
+    A = inputs.random_fp16((M, K), 87).pin_memory()
+    B = inputs.random_fp16((K, N), 88).pin_memory()
+    bias = inputs.random_fp16((N,), 89).pin_memory()
+    C = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+    g.gemm_set_debug(ctx, FORCE["splitk"])
+    try:
+        g.gemm_run_host(ctx, M, N, K, A, B, bias, C, g.EPI_GELU)
+    finally:
+        g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
+    assert bool(torch.isfinite(C).all())
+    rows = inputs.sample_rows(M, 200, seed=10, include_last=4).numpy()
+    assert_parity(C.numpy()[rows], oracle_ref(A, B, bias, g.EPI_GELU, rows=rows), "split-K column bands")
+
+
 def test_streamk_graph_replays_with_new_inputs(ctx):
     """A captured stream-K GEMM replayed with new inputs each time: every owner must wait for
     this replay's partials (the flags are lowered after use, not left from the last run)."""
@@ -422,10 +491,13 @@ def test_streamk_graph_replays_with_new_inputs(ctx):
         g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
 
 
-def test_default_streamk_on_few_tiles(ctx):
-    """1024 x 1024 x 8192 + bias + GELU on the default schedule: 32 tiles of 128 x 256 on
-    ~150 SMs take stream-K (each tile cut into ~5 parts). Against the oracle on sampled
-    rows, and bit-identical between two runs (the parts are added in a fixed order)."""
+@pytest.mark.parametrize("schedule", ["default", "streamk"])
+def test_default_streamk_on_few_tiles(ctx, schedule):
+    """1024 x 1024 x 8192 + bias + GELU: 32 tiles of 128 x 256 on ~150 SMs. The default
+    schedule takes split-K (clusters of 4 CTAs, each a quarter of K); forced stream-K cuts
+    each tile into ~5 parts. Against the oracle on sampled rows, and bit-identical between
+    two runs (the parts are added in a fixed order)."""
+    g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE if schedule == "default" else FORCE["streamk"])
     M, N, K = 1024, 1024, 8192
     A = inputs.random_fp16((M, K), 61, "normal")
     B = inputs.random_fp16((K, N), 62, "normal_inv_k", k=K)
@@ -441,7 +513,8 @@ def test_default_streamk_on_few_tiles(ctx):
     assert torch.equal(C1, C2)
     rows = inputs.sample_rows(M, 96, seed=5, include_last=2).numpy()
     rows = np.union1d(rows, [0, 127, 128, 511, 512, 1023])
-    assert_parity(C1.cpu().numpy()[rows], oracle_ref(A, B, bias, g.EPI_GELU, rows=rows), "stream-K default")
+    g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
+    assert_parity(C1.cpu().numpy()[rows], oracle_ref(A, B, bias, g.EPI_GELU, rows=rows), f"few tiles, {schedule}")
 
 
 def test_host_buffer_entry_point(ctx):
