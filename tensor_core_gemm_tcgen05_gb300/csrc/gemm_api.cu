@@ -30,6 +30,10 @@ using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS>;
 // small K), and the whole-tile kernel when all tiles fit one wave, where every CTA's
 // epilogue is an exposed tail that twice the warps shorten (2048^3: 15.6 -> 15.0 us).
 using Cfg8 = gb300::KernelConfig<128, 256, 3, 8>;
+// Split-K runs on the eight-warp instance: twice the warps to stage the partial and to
+// read the other CTAs' partials over DSMEM (measured 2-5 % faster than four on 5 of 6
+// few-tile shapes); its 3-stage ring (144 KB) holds the 128 KB partial.
+using SplitCfg = Cfg8;
 #ifndef GB300_GROUP_PANEL_MB
 #define GB300_GROUP_PANEL_MB 32
 #endif
@@ -326,8 +330,8 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
         }
         if (split > 0) {
             p.split = split;
-            launch_pdl_cluster(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_SPLIT_K>, p.num_tiles * split, split,
-                               Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
+            launch_pdl_cluster(gb300::gemm_tcgen05_kernel<SplitCfg, gb300::SCHED_SPLIT_K>, p.num_tiles * split, split,
+                               SplitCfg::NUM_THREADS, SplitCfg::SMEM_BYTES, stream, ta, tb, tc, p);
             const cudaError_t e = cudaGetLastError();
             return e == cudaSuccess ? GEMM_OK : cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
         }
@@ -440,13 +444,13 @@ int gemm_create(gemm_ctx **out, int device)
     // Split-K clusters: how many clusters of 2, 4 and 8 CTAs fit at once (0: that size is not
     // used).
     {
-        auto *sk = gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_SPLIT_K>;
-        if (cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) == cudaSuccess) {
+        auto *sk = gb300::gemm_tcgen05_kernel<SplitCfg, gb300::SCHED_SPLIT_K>;
+        if (cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SplitCfg::SMEM_BYTES) == cudaSuccess) {
             for (int cs = 2; cs <= 8; cs *= 2) {
                 cudaLaunchConfig_t lc = {};
                 lc.gridDim = dim3(static_cast<unsigned>(cs * (sms / cs)), 1, 1);
-                lc.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
-                lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+                lc.blockDim = dim3(SplitCfg::NUM_THREADS, 1, 1);
+                lc.dynamicSmemBytes = SplitCfg::SMEM_BYTES;
                 cudaLaunchAttribute a[1];
                 a[0].id = cudaLaunchAttributeClusterDimension;
                 a[0].val.clusterDim.x = static_cast<unsigned>(cs);

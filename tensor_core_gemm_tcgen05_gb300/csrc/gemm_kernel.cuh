@@ -861,24 +861,24 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t tadd
     }
 }
 
-// Split-K, step 1: an epilogue warp copies its 32 accumulator rows (all BN columns) into the
-// CTA's staging area (the idle operand ring): FP32 row r at r * BN * 4 bytes, its 16-byte
-// unit u stored at unit u ^ (r & 7), so that the eight lanes of a quarter-warp, eight
-// consecutive rows, write eight different bank groups.
-template <int BN>
-__device__ __forceinline__ void splitk_stage(uint32_t taddr, uint32_t stage_base, int row, int lane)
+// Split-K, step 1: an epilogue warp copies its 32 accumulator rows (CHUNKS 32-column chunks
+// from chunk c_begin on, TMEM address `taddr` = chunk c_begin) into the CTA's staging area
+// (the idle operand ring): FP32 row r at r * BN * 4 bytes, its 16-byte unit u stored at unit
+// u ^ (r & 7), so that the eight lanes of a quarter-warp, eight consecutive rows, write eight
+// different bank groups.
+template <int BN, int CHUNKS>
+__device__ __forceinline__ void splitk_stage(uint32_t taddr, uint32_t stage_base, int row, int c_begin)
 {
-    (void)lane;
     const uint32_t row_addr = stage_base + static_cast<uint32_t>(row) * (BN * 4);
     const uint32_t sw = static_cast<uint32_t>(row & 7);
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = 0; c < CHUNKS; ++c) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + 32u * static_cast<uint32_t>(c), v);
         tmem_ld_wait_regs(v);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            st_shared_v4(row_addr + (((static_cast<uint32_t>(8 * c + j)) ^ sw) << 4),
+            st_shared_v4(row_addr + (((static_cast<uint32_t>(8 * (c_begin + c) + j)) ^ sw) << 4),
                          make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
     }
 }
@@ -892,15 +892,16 @@ __device__ __forceinline__ void splitk_stage(uint32_t taddr, uint32_t stage_base
 // issued before the current one is added); the S partials are added in rank order, so the
 // result does not depend on timing. Then bias, activation, FP16 (rows past M and columns past
 // N are skipped; N is a multiple of 8, so a unit is either inside C or past it).
-template <int BM, int BN, int S>
+template <int BM, int BN, int WARPS, int S>
 __device__ __forceinline__ void splitk_reduce_s(const GemmParams &p, uint32_t stage_base, int mb, int nb, int rank,
                                                 int tid)
 {
     static_assert(BN == 256 && BM == 128, "two 16-byte units per lane per row");
     constexpr int R = BM / S;
-    constexpr int ROWS_W = R / 4;                 // rows per warp
+    constexpr int ROWS_W = R / WARPS;             // rows per warp
     constexpr int ROWS_B = 8 / S;                 // rows per batch (16 loads per lane)
-    constexpr int BATCHES = ROWS_W / ROWS_B;      // 4
+    constexpr int BATCHES = ROWS_W / ROWS_B;      // 4 with four warps, 2 with eight
+    static_assert(BATCHES >= 1 && ROWS_W % ROWS_B == 0, "whole batches per warp");
     const int w = tid >> 5, lane = tid & 31;
     const int r0 = rank * R + w * ROWS_W;         // first tile row of this warp
     uint32_t src[S];
@@ -971,16 +972,16 @@ __device__ __forceinline__ void splitk_reduce_s(const GemmParams &p, uint32_t st
     }
 }
 
-template <int BM, int BN>
+template <int BM, int BN, int WARPS>
 __device__ __forceinline__ void splitk_reduce(const GemmParams &p, uint32_t stage_base, int mb, int nb, int rank,
                                               int tid)
 {
     if (p.split == 8)
-        splitk_reduce_s<BM, BN, 8>(p, stage_base, mb, nb, rank, tid);
+        splitk_reduce_s<BM, BN, WARPS, 8>(p, stage_base, mb, nb, rank, tid);
     else if (p.split == 4)
-        splitk_reduce_s<BM, BN, 4>(p, stage_base, mb, nb, rank, tid);
+        splitk_reduce_s<BM, BN, WARPS, 4>(p, stage_base, mb, nb, rank, tid);
     else
-        splitk_reduce_s<BM, BN, 2>(p, stage_base, mb, nb, rank, tid);
+        splitk_reduce_s<BM, BN, WARPS, 2>(p, stage_base, mb, nb, rank, tid);
 }
 
 // SCHED: SCHED_TILES (whole tiles per CTA), SCHED_STREAM_K (p.sk_units > 0, workspace and
@@ -1174,8 +1175,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if constexpr (SCHED == SCHED_SPLIT_K) {
             // this CTA's partial sum of its tile into the staging area; the cluster reduces
             // the partials after the barrier below
-            static_assert(Cfg::EPI_COL_GROUPS == 1 && BM * BN * 4 <= Cfg::STAGES * Cfg::STAGE_BYTES,
-                          "one warp per lane quarter; the staged partial fits the operand ring");
+            static_assert(BM * BN * 4 <= Cfg::STAGES * Cfg::STAGE_BYTES, "the staged partial fits the operand ring");
             WorkIter<SCHED> work(p);
             int t, mb, nb, k0, k1;
             if (work.next(p, t, mb, nb, k0, k1)) {
@@ -1184,7 +1184,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     ok = wait_bounded(accf0, 0u, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
                 if (__shfl_sync(0xffffffffu, ok, 0)) {
                     tc_fence_after_sync();
-                    splitk_stage<BN>(tmem_base + lane_base, sA, quarter * 32 + lane, lane);
+                    splitk_stage<BN, CHUNKS>(tmem_base + lane_base + static_cast<uint32_t>(c_begin * 32), sA,
+                                             quarter * 32 + lane, c_begin);
                 }
             }
         } else if constexpr (SCHED == SCHED_ROW_CLUSTER) {
@@ -1353,8 +1354,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             WorkIter<SCHED> work(p);
             int t, mb, nb, k0, k1;
             if (work.next(p, t, mb, nb, k0, k1) && *abort_flag == 0)
-                splitk_reduce<BM, BN>(p, sA, mb, nb, static_cast<int>(cluster_ctarank()),
-                                      static_cast<int>(threadIdx.x) - 64);
+                splitk_reduce<BM, BN, Cfg::NUM_EPI_WARPS>(p, sA, mb, nb, static_cast<int>(cluster_ctarank()),
+                                                          static_cast<int>(threadIdx.x) - 64);
         }
         cluster_sync();   // no CTA leaves while another may still read its partial
     }
