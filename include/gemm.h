@@ -118,9 +118,10 @@ int gemm_run(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, cons
  * streams and their events are owned by the context (created or grown on first use, freed
  * by gemm_destroy). Outputs under 32 MiB are done in one piece; larger ones in 4 bands (8
  * from 256 MiB on) of whole 256-wide tiles whose uploads, GEMMs (one kernel launch each, on `stream`)
- * and downloads overlap: column bands of C when A is the smaller operand (A goes first,
- * whole, then B in column bands), row bands otherwise (B whole, then A in row bands); the
- * softmax epilogue always uses row bands. Returns after C is on the host (the call
+ * and downloads overlap: column bands of C when A is the smaller operand (A in two row halves
+ * when it is 32 MiB or more, uploaded in the order the GEMMs need them: A_0, B_0, A_1, B_1,
+ * B_2, ..., one GEMM per row half and column band), row bands otherwise (B whole, then A in
+ * row bands); the softmax epilogue always uses row bands. Returns after C is on the host (the call
  * synchronises `stream`). Same argument rules as gemm_run, except that the pointers are
  * host pointers. Also reports a device-side timeout (GEMM_ERR_TIMEOUT), since it
  * synchronises. */

@@ -53,8 +53,9 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int64_t kSoftmaxMaxCtas = int64_t(1) << 20;   // row softmax grid cap (CTAs loop past it)
 constexpr int kSoftmaxTileN = 256;    // columns of C per CTA of a softmax row cluster
 constexpr int kRowClusterMax = 16;    // clusters of up to 16 CTAs (N <= 4096)
-// gemm_run_host splits M into at most this many chunks whose uploads, GEMMs and downloads
-// overlap; outputs smaller than kHostChunkMinBytes are not split.
+// gemm_run_host splits C into at most this many bands (column bands: also two row halves of
+// A when A is at least kHostChunkMinBytes) whose uploads, GEMMs and downloads overlap;
+// outputs smaller than kHostChunkMinBytes are not split.
 constexpr int kHostChunksMax = 8;
 constexpr size_t kHostChunkMinBytes = size_t(32) << 20;
 constexpr uint64_t kMinTimeoutNs = 1000000ull;
@@ -94,7 +95,7 @@ struct gemm_ctx {
     size_t stage_bytes = 0;
     cudaStream_t copy_in = nullptr, copy_out = nullptr;
     cudaEvent_t ev_start = nullptr, ev_done = nullptr;
-    cudaEvent_t ev_in[kHostChunksMax] = {}, ev_mm[kHostChunksMax] = {};
+    cudaEvent_t ev_in[2 * kHostChunksMax] = {}, ev_mm[2 * kHostChunksMax] = {};
 };
 
 namespace {
@@ -559,7 +560,7 @@ int gemm_run_host(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A,
             e = cudaEventCreateWithFlags(&ctx->ev_start, cudaEventDisableTiming);
         if (e == cudaSuccess)
             e = cudaEventCreateWithFlags(&ctx->ev_done, cudaEventDisableTiming);
-        for (int i = 0; i < kHostChunksMax && e == cudaSuccess; ++i) {
+        for (int i = 0; i < 2 * kHostChunksMax && e == cudaSuccess; ++i) {
             e = cudaEventCreateWithFlags(&ctx->ev_in[i], cudaEventDisableTiming);
             if (e == cudaSuccess)
                 e = cudaEventCreateWithFlags(&ctx->ev_mm[i], cudaEventDisableTiming);
@@ -605,29 +606,65 @@ int gemm_run_host(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A,
         int64_t cols = (N + parts - 1) / parts;
         cols = (cols + 255) / 256 * 256;   // whole 256-column tiles
         const int bands = static_cast<int>((N + cols - 1) / cols);
-        if (a_b && (e = cudaMemcpyAsync(dA, A, a_b, cudaMemcpyHostToDevice, ctx->copy_in)) != cudaSuccess)
-            return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+        // A large A is also cut in two row halves (the first of whole 256-row tiles), so that
+        // the first GEMM needs half of A and one band of B, not all of A, before the first
+        // download can start. Uploads go once each, in the order the GEMMs need them: A_0,
+        // B_0, A_1, B_1, B_2, ...; GEMM (i, j) waits for A_i and B_j.
+        int64_t rows_h = M;
+        if (a_b >= kHostChunkMinBytes) {
+            const int64_t h = (M / 2 + 255) / 256 * 256;
+            if (h < M)
+                rows_h = h;
+        }
+        const int halves = rows_h < M ? 2 : 1;
         const size_t pitch = static_cast<size_t>(N) * 2;
+        cudaEvent_t *ev_a = ctx->ev_in, *ev_b = ctx->ev_in + 2;   // after A_i, after B_j
+        auto upload_a = [&](int i) -> cudaError_t {
+            const int64_t r0 = i * rows_h, mi = std::min<int64_t>(rows_h, M - r0);
+            const size_t off = static_cast<size_t>(r0) * K * 2, len = static_cast<size_t>(mi) * K * 2;
+            cudaError_t err = len ? cudaMemcpyAsync(dA + off, static_cast<const char *>(A) + off, len,
+                                                    cudaMemcpyHostToDevice, ctx->copy_in)
+                                  : cudaSuccess;
+            return err == cudaSuccess ? cudaEventRecord(ev_a[i], ctx->copy_in) : err;
+        };
+        auto upload_b = [&](int j) -> cudaError_t {
+            const int64_t c0 = j * cols, nj = std::min<int64_t>(cols, N - c0);
+            const size_t off = static_cast<size_t>(c0) * 2;
+            cudaError_t err = K > 0 ? cudaMemcpy2DAsync(dB + off, pitch, static_cast<const char *>(B) + off, pitch,
+                                                        static_cast<size_t>(nj) * 2, static_cast<size_t>(K),
+                                                        cudaMemcpyHostToDevice, ctx->copy_in)
+                                    : cudaSuccess;
+            return err == cudaSuccess ? cudaEventRecord(ev_b[j], ctx->copy_in) : err;
+        };
+        if ((e = upload_a(0)) != cudaSuccess || (e = upload_b(0)) != cudaSuccess ||
+            (halves == 2 && (e = upload_a(1)) != cudaSuccess))
+            return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+        for (int j = 1; j < bands; ++j)
+            if ((e = upload_b(j)) != cudaSuccess)
+                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+        int k = 0;
         for (int j = 0; j < bands; ++j) {
             const int64_t c0 = j * cols, nj = std::min<int64_t>(cols, N - c0);
             const size_t off = static_cast<size_t>(c0) * 2, width = static_cast<size_t>(nj) * 2;
-            if (K > 0 && (e = cudaMemcpy2DAsync(dB + off, pitch, static_cast<const char *>(B) + off, pitch, width,
-                                                static_cast<size_t>(K), cudaMemcpyHostToDevice, ctx->copy_in)) !=
-                             cudaSuccess)
-                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
-            if ((e = cudaEventRecord(ctx->ev_in[j], ctx->copy_in)) != cudaSuccess ||
-                (e = cudaStreamWaitEvent(s, ctx->ev_in[j], 0)) != cudaSuccess)
-                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
-            rc = launch(ctx, static_cast<int>(M), static_cast<int>(nj), static_cast<int>(K), K ? dA : nullptr,
-                        K ? dB + off : nullptr, dbias ? dbias + off : nullptr, dC + off, epilogue, s, N, N);
-            if (rc != GEMM_OK)
-                return rc;
-            if ((e = cudaEventRecord(ctx->ev_mm[j], s)) != cudaSuccess ||
-                (e = cudaStreamWaitEvent(ctx->copy_out, ctx->ev_mm[j], 0)) != cudaSuccess)
-                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
-            if ((e = cudaMemcpy2DAsync(static_cast<char *>(C) + off, pitch, dC + off, pitch, width,
-                                       static_cast<size_t>(M), cudaMemcpyDeviceToHost, ctx->copy_out)) != cudaSuccess)
-                return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+            for (int i = 0; i < halves; ++i, ++k) {
+                const int64_t r0 = i * rows_h, mi = std::min<int64_t>(rows_h, M - r0);
+                const size_t a_off = static_cast<size_t>(r0) * K * 2, c_off = static_cast<size_t>(r0) * pitch + off;
+                if ((e = cudaStreamWaitEvent(s, ev_a[i], 0)) != cudaSuccess ||
+                    (e = cudaStreamWaitEvent(s, ev_b[j], 0)) != cudaSuccess)
+                    return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+                rc = launch(ctx, static_cast<int>(mi), static_cast<int>(nj), static_cast<int>(K),
+                            K ? dA + a_off : nullptr, K ? dB + off : nullptr, dbias ? dbias + off : nullptr,
+                            dC + c_off, epilogue, s, N, N);
+                if (rc != GEMM_OK)
+                    return rc;
+                if ((e = cudaEventRecord(ctx->ev_mm[k], s)) != cudaSuccess ||
+                    (e = cudaStreamWaitEvent(ctx->copy_out, ctx->ev_mm[k], 0)) != cudaSuccess)
+                    return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+                if ((e = cudaMemcpy2DAsync(static_cast<char *>(C) + c_off, pitch, dC + c_off, pitch, width,
+                                           static_cast<size_t>(mi), cudaMemcpyDeviceToHost, ctx->copy_out)) !=
+                    cudaSuccess)
+                    return cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+            }
         }
     } else {
         int64_t rows = (M + parts - 1) / parts;
@@ -699,7 +736,7 @@ int gemm_destroy(gemm_ctx *ctx)
             cudaFree(ctx->sk_flags);
         if (ctx->stage)
             cudaFree(ctx->stage);
-        for (int i = 0; i < kHostChunksMax; ++i) {
+        for (int i = 0; i < 2 * kHostChunksMax; ++i) {
             if (ctx->ev_in[i])
                 cudaEventDestroy(ctx->ev_in[i]);
             if (ctx->ev_mm[i])

@@ -552,6 +552,23 @@ def test_host_buffer_entry_point(ctx):
     assert_parity(C.numpy()[rows], oracle_ref(A, B, bias, g.EPI_RELU, rows=rows), "gemm_run_host column bands")
 
 
+def test_host_buffer_row_halves_and_column_bands(ctx):
+    """gemm_run_host with A of 33.6 MB (at least 32 MiB) and smaller than B: A goes up in two
+    row halves (2304 rows, then 1800) and B in four column bands, one GEMM per half and band
+    (eight GEMMs, each writing a slice of C with row stride N). Sampled rows on both sides of
+    the halves' boundary, against the oracle."""
+    M, N, K = 4104, 8200, 4096
+    A = inputs.random_fp16((M, K), 91, "normal").pin_memory()
+    B = inputs.random_fp16((K, N), 92, "normal_inv_k", k=K).pin_memory()
+    bias = inputs.random_fp16((N,), 93).pin_memory()
+    C = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+    g.gemm_run_host(ctx, M, N, K, A, B, bias, C, g.EPI_GELU)
+    assert bool(torch.isfinite(C).all())
+    rows = inputs.sample_rows(M, 120, seed=11, include_last=4).numpy()
+    rows = np.union1d(rows, [0, 2303, 2304, 2305])
+    assert_parity(C.numpy()[rows], oracle_ref(A, B, bias, g.EPI_GELU, rows=rows), "row halves x column bands")
+
+
 def test_side_stream_and_cuda_graph(ctx):
     dev = torch.device("cuda:0")
     M, N, K = 640, 768, 512
