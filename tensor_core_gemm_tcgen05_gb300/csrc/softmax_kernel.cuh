@@ -12,10 +12,11 @@
 //    vectors of the row at once (all loads in flight together, which is what keeps HBM busy)
 //    and keeps them in registers; the maximum is taken on the FP16 values (exact), then the
 //    sum of exp(x - m), then the outputs, all from the registers: X is read once.
-//  * Longer rows (row_softmax_kernel): pass 1 streams the row with 16-byte loads and keeps,
-//    per thread, a running maximum m and a sum s of exp(x - m) that is rescaled whenever m
-//    grows (the "online" form, so the row is read once for both statistics); pass 2 reads
-//    the row again and writes exp(x - m) * (1 / s) with 16-byte stores.
+//  * Longer rows (row_softmax_kernel): pass 1 reads the row once with 16-byte loads, keeping
+//    per thread a running maximum m and a sum s of exp(x - m) that is rescaled whenever m
+//    grows (the "online" form), and each thread's first 16 vectors in registers and shared
+//    memory; pass 2 writes exp(x - m) * (1 / s) from those and reads only the rest of the
+//    row again (rows of up to 32768 columns are read once).
 // The (m, s) statistics of a group are merged with warp shuffles (and shared memory across
 // the warps of a CTA).
 #pragma once
@@ -151,89 +152,110 @@ __global__ void __launch_bounds__(G < 256 ? 256 : G, MIN_CTAS)
     }
 }
 
-template <int G>   // threads per row: 32 (one warp) or a multiple of 32 up to the block size
+// Running (max, sum of exp(x - max)) of a row piece, updated with N more 16-byte vectors
+// (vectors past the row's end are -inf and add nothing): the vectors' maximum in FP16
+// (exact), the old sum rescaled once. Nothing changes while every value so far is -inf.
+template <int N>
+__device__ __forceinline__ void online_update(float &m, float &s, const uint4 (&q)[N])
+{
+    __half2 hm = u32_as_half2(0xFC00FC00u);
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        hm = hmax_vec(hm, q[i]);
+    const float mn = fmaxf(m, fmaxf(__low2float(hm), __high2float(hm)));
+    if (mn == -INFINITY)
+        return;
+    const float mb = mn * kLog2e;
+    float add = 0.0f;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        add += (exp_pair_sum(q[i].x, mb) + exp_pair_sum(q[i].y, mb)) +
+               (exp_pair_sum(q[i].z, mb) + exp_pair_sum(q[i].w, mb));
+    s = s * ex2_approx((m - mn) * kLog2e) + add;   // m = -inf at first: the product is 0
+    m = mn;
+}
+
+// Rows longer than row_softmax_regs_kernel takes (above 16384 columns): a 256-thread CTA per
+// row, walked by a persistent grid. Pass 1 reads the row once, keeping each thread's first
+// RV vectors in registers and its next SV in shared memory ([i][thread]: each thread reads
+// back only what it wrote, so no barrier), and updates a running (max, rescaled sum); the
+// CTA's statistics are merged with warp shuffles and shared memory; pass 2 writes exp(x - m)
+// / s from registers, then from shared memory, and re-reads only the part of the row past
+// (RV + SV) * 256 vectors (rows of up to 32768 columns are read once).
+template <int G>
 __global__ void __launch_bounds__(256) row_softmax_kernel(const __half *__restrict__ X, __half *__restrict__ Y,
                                                           int64_t rows, int cols)
 {
-    static_assert(G == 32 || G == 256, "a warp or the whole block per row");
-    constexpr int GROUPS = 256 / G;            // rows in flight per block
+    static_assert(G == 256, "the whole block per row");
+    constexpr int RV = 8, SV = 8;
+    __shared__ uint4 cache[SV][G];
     __shared__ float red_m[8], red_s[8];
-    const int group = threadIdx.x / G;
-    const int t = threadIdx.x % G;             // thread within the row group
-    const int lane = threadIdx.x & 31;
+    const int t = threadIdx.x;
+    const int lane = t & 31;
     const int vecs = cols / 8;                 // 16-byte vectors per row
+    const uint4 neg = make_uint4(0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u);   // -inf
 
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * GROUPS + group; r < rows;
-         r += static_cast<int64_t>(gridDim.x) * GROUPS) {
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const uint4 *xr = reinterpret_cast<const uint4 *>(X + r * cols);
         uint4 *yr = reinterpret_cast<uint4 *>(Y + r * cols);
 
-        // pass 1: running max and rescaled sum of exponentials
+        // pass 1
         float m = -INFINITY, s = 0.0f;
-        for (int v = t; v < vecs; v += G) {
-            const uint4 q = __ldg(xr + v);
-            const __half2 *h = reinterpret_cast<const __half2 *>(&q);
-            float f[8];
+        uint4 q[RV];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 p = __half22float2(h[e]);
-                f[2 * e] = p.x;
-                f[2 * e + 1] = p.y;
-            }
-            float vm = f[0];
+        for (int i = 0; i < RV; ++i)
+            q[i] = t + i * G < vecs ? __ldcs(xr + t + i * G) : neg;
+        {
+            uint4 c[SV];
 #pragma unroll
-            for (int e = 1; e < 8; ++e)
-                vm = fmaxf(vm, f[e]);
-            const float mn = fmaxf(m, vm);
-            if (mn == -INFINITY)
-                continue;   // everything so far is -inf: nothing to add yet
-            float add = 0.0f;
+            for (int i = 0; i < SV; ++i)
+                c[i] = t + (RV + i) * G < vecs ? __ldcs(xr + t + (RV + i) * G) : neg;
+            online_update<RV>(m, s, q);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                add += exp2f((f[e] - mn) * kLog2e);
-            s = s * exp2f((m - mn) * kLog2e) + add;   // m = -inf at first: exp2f(-inf) = 0
-            m = mn;
+            for (int i = 0; i < SV; ++i)
+                cache[i][t] = c[i];
+            online_update<SV>(m, s, c);
         }
-        // merge within the warp
+        for (int v = t + (RV + SV) * G; v < vecs; v += G) {
+            const uint4 c[1] = {__ldg(xr + v)};   // read again in pass 2: keep it in L2
+            online_update<1>(m, s, c);
+        }
+        // merge within the warp, then across the warps of the block
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
             const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
             softmax_merge(m, s, m2, s2);
         }
-        if constexpr (G > 32) {   // merge across the warps of the block
-            const int warp = threadIdx.x >> 5;
-            __syncthreads();      // the previous row's reads of red_* are done
-            if (lane == 0) {
-                red_m[warp] = m;
-                red_s[warp] = s;
-            }
-            __syncthreads();
-            m = red_m[0];
-            s = red_s[0];
-#pragma unroll
-            for (int w = 1; w < G / 32; ++w)
-                softmax_merge(m, s, red_m[w], red_s[w]);
+        __syncthreads();   // the previous row's reads of red_* are done
+        if (lane == 0) {
+            red_m[t >> 5] = m;
+            red_s[t >> 5] = s;
         }
+        __syncthreads();
+        m = red_m[0];
+        s = red_s[0];
+#pragma unroll
+        for (int w = 1; w < G / 32; ++w)
+            softmax_merge(m, s, red_m[w], red_s[w]);
         const float inv = 1.0f / s;
         const float mb = m * kLog2e;
 
-        // pass 2: write exp(x - m) / s
-        for (int v = t; v < vecs; v += G) {
-            const uint4 q = __ldg(xr + v);
-            const __half2 *h = reinterpret_cast<const __half2 *>(&q);
-            uint4 out;
-            uint32_t *o = reinterpret_cast<uint32_t *>(&out);
+        // pass 2: exp(x - m) / s
+        auto out = [&](const uint4 &x) {
+            return make_uint4(softmax_pair(x.x, mb, inv), softmax_pair(x.y, mb, inv), softmax_pair(x.z, mb, inv),
+                              softmax_pair(x.w, mb, inv));
+        };
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 p = __half22float2(h[e]);
-                const float a = exp2f(fmaf(p.x, kLog2e, -mb)) * inv;
-                const float b = exp2f(fmaf(p.y, kLog2e, -mb)) * inv;
-                __half2 hh = __floats2half2_rn(a, b);
-                o[e] = *reinterpret_cast<uint32_t *>(&hh);
-            }
-            __stcs(yr + v, out);
-        }
+        for (int i = 0; i < RV; ++i)
+            if (t + i * G < vecs)
+                __stcs(yr + t + i * G, out(q[i]));
+#pragma unroll
+        for (int i = 0; i < SV; ++i)
+            if (t + (RV + i) * G < vecs)
+                __stcs(yr + t + (RV + i) * G, out(cache[i][t]));
+        for (int v = t + (RV + SV) * G; v < vecs; v += G)
+            __stcs(yr + v, out(__ldg(xr + v)));
     }
 }
 
