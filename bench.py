@@ -376,25 +376,32 @@ def measure_attention(g, ctx, stream, device, peaks, steps=10):
     return out
 
 
-def measure_e2e(g, ctx, w, host, stream, steps):
+def measure_e2e(g, ctx, w, host, stream, steps, batches=3):
     """Same metric through gemm_run_host: pinned host inputs copied in, C copied out, every
-    step inside the timed region (host wall clock around synchronous calls)."""
+    step inside the timed region (host wall clock around synchronous calls). `batches` timed
+    batches of `steps` calls; the median batch is reported (a batch of a few milliseconds is
+    easily disturbed on the host side), every batch's value alongside."""
     import torch
     A, B, bias = host
     pA, pB = A.pin_memory(), B.pin_memory()
     pbias = bias.pin_memory() if bias is not None else None
     pC = torch.empty(w.M, w.N, dtype=torch.float16).pin_memory()
-    for _ in range(2):
+    for _ in range(3):
         g.gemm_run_host(ctx, w.M, w.N, w.K, pA, pB, pbias, pC, w.epi_code, stream)
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        g.gemm_run_host(ctx, w.M, w.N, w.K, pA, pB, pbias, pC, w.epi_code, stream)
-    dt = time.perf_counter() - t0
+    dts = []
+    for _ in range(batches):
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            g.gemm_run_host(ctx, w.M, w.N, w.K, pA, pB, pbias, pC, w.epi_code, stream)
+        dts.append(time.perf_counter() - t0)
+    dt = statistics.median(dts)
     h2d = 2 * (w.M * w.K + w.K * w.N) + (2 * w.N if w.bias else 0)
     d2h = 2 * w.M * w.N
     return {"value": round(w.flops * steps / dt / 1e12, 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": round(dt * 1e3 / steps, 4), "api": "gemm_run_host (pinned host buffers)"}
+            "ms_per_step": round(dt * 1e3 / steps, 4),
+            "batches": [round(w.flops * steps / t / 1e12, 1) for t in dts],
+            "api": "gemm_run_host (pinned host buffers)"}
 
 
 def cpu_baseline(w, host, target_s=12.0, max_rows=None):

@@ -861,8 +861,12 @@ int gemm_row_softmax(gemm_ctx *ctx, int64_t rows, int64_t cols, const void *X, v
     const __half *x = static_cast<const __half *>(X);
     __half *y = static_cast<__half *>(Y);
     // Rows held in registers (see launch_softmax_regs): a warp per row up to 2048 columns, a
-    // 256-thread CTA per row up to 16384. Longer rows are streamed twice (measured faster than
-    // 16 vectors per thread at one CTA per SM: the row's loads and arithmetic cannot overlap).
+    // 256-thread CTA per row up to 16384. Where it measured faster, the CTAs per SM are as
+    // many as the registers allow without spilling (3 at 8 vectors per thread: 80 registers;
+    // 5 at 4 with a CTA per row: 48), since the bytes in flight per SM are what keep HBM busy
+    // (three rows of 16384 per SM instead of two: 88 -> 79 us at 8192 rows). Longer rows go
+    // to the streaming kernel (faster than 16 vectors per thread at one CTA per SM: the row's
+    // loads and arithmetic cannot overlap).
     if (cols <= 256)
         launch_softmax_regs<32, 1, 8>(rows, c, x, y, st);
     else if (cols <= 512)
@@ -870,14 +874,14 @@ int gemm_row_softmax(gemm_ctx *ctx, int64_t rows, int64_t cols, const void *X, v
     else if (cols <= 1024)
         launch_softmax_regs<32, 4, 4>(rows, c, x, y, st);
     else if (cols <= 2048)
-        launch_softmax_regs<32, 8, 2>(rows, c, x, y, st);
+        launch_softmax_regs<32, 8, 3>(rows, c, x, y, st);
     else if (cols <= 4096)
         launch_softmax_regs<256, 2, 8>(rows, c, x, y, st);
     else if (cols <= 8192)
-        launch_softmax_regs<256, 4, 4>(rows, c, x, y, st);
+        launch_softmax_regs<256, 4, 5>(rows, c, x, y, st);
     else if (cols <= 16384)
-        launch_softmax_regs<256, 8, 2>(rows, c, x, y, st);
-    else {   // longer rows: streamed twice
+        launch_softmax_regs<256, 8, 3>(rows, c, x, y, st);
+    else {   // longer rows: streamed (read once up to 32768 columns)
         const int64_t blocks = std::min<int64_t>(rows, static_cast<int64_t>(ctx->num_sms) * 8);
         gb300::row_softmax_kernel<256><<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, y, rows, c);
     }
