@@ -83,3 +83,21 @@ def test_peaks_fall_back_when_measurements_are_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     peaks, src = bench.load_peaks()
     assert src == "fallback" and peaks["bf16_tflops"] == 1900.0
+
+
+def test_end_to_end_figure_counts_every_call_and_its_bytes(monkeypatch):
+    """The host-buffer figure: warm-up calls, then three timed batches of `steps` calls, each
+    call one whole GEMM with its copies; the bytes per step are the inputs and C."""
+    import types
+    monkeypatch.setattr(torch.Tensor, "pin_memory", lambda self, *a, **k: self)
+    w = types.SimpleNamespace(M=64, N=32, K=16, bias=True, epi_code=1, flops=2 * 64 * 32 * 16)
+    calls = []
+    g = types.SimpleNamespace(gemm_run_host=lambda *a: calls.append(a))
+    host = (torch.zeros(64, 16, dtype=torch.float16), torch.zeros(16, 32, dtype=torch.float16),
+            torch.zeros(32, dtype=torch.float16))
+    r = bench.measure_e2e(g, None, w, host, None, steps=10)
+    assert len(calls) == 3 + 3 * 10
+    assert len(r["batches"]) == 3 and r["steps"] == 10
+    assert r["h2d_bytes_per_step"] == 2 * (64 * 16 + 16 * 32) + 2 * 32
+    assert r["d2h_bytes_per_step"] == 2 * 64 * 32
+    assert min(r["batches"]) - 0.1 <= r["value"] <= max(r["batches"]) + 0.1   # batches rounded to 0.1
