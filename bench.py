@@ -178,6 +178,113 @@ class ClockSampler:
         }
 
 
+class NvmlSampler:
+    """In-process, query-only NVML polling (SM clock, power, clock-event reasons) on a
+    background thread, every `period_s` seconds, each sample stamped with the host's
+    perf_counter. ctypes releases the GIL during each NVML call, so the launching thread is
+    not held up. `summary(t0, t1)` describes the samples inside a host-time window."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    FI_POWER_INSTANT = 186   # NVML field id of the instantaneous board power (mW)
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        import ctypes
+        import threading
+        import torch
+        self.ct = ctypes
+        self.period = period_s
+        self.samples = []   # (t, sm_mhz, power_w, reason_mask, call_us)
+        self.L = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.L.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        self.h = ctypes.c_void_p()
+        if self.L.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError(f"no NVML handle for {uuid}")
+        mx = ctypes.c_uint(0)
+        rc = self.L.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.sm_max = float(mx.value) if rc == 0 else None
+
+        class Value(ctypes.Union):
+            _fields_ = [("dVal", ctypes.c_double), ("uiVal", ctypes.c_uint), ("ulVal", ctypes.c_ulong),
+                        ("ullVal", ctypes.c_ulonglong), ("sllVal", ctypes.c_longlong), ("siVal", ctypes.c_int),
+                        ("usVal", ctypes.c_ushort)]
+
+        class Field(ctypes.Structure):
+            _fields_ = [("fieldId", ctypes.c_uint32), ("scopeId", ctypes.c_uint32), ("timestamp", ctypes.c_int64),
+                        ("latencyUsec", ctypes.c_int64), ("valueType", ctypes.c_uint), ("nvmlReturn", ctypes.c_uint),
+                        ("value", Value)]
+
+        self.field = Field()
+        self.power_source = "instant"
+        if not self._power_instant():
+            self.power_source = "average"
+        self.stop_ev = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _power_instant(self):
+        f = self.field
+        f.fieldId = self.FI_POWER_INSTANT
+        f.scopeId = 0
+        if self.L.nvmlDeviceGetFieldValues(self.h, 1, self.ct.byref(f)) != 0 or f.nvmlReturn != 0:
+            return None
+        return f.value.uiVal / 1000.0
+
+    def _sample(self):
+        ct = self.ct
+        t = time.perf_counter()
+        clk, mw, reasons = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        rc = self.L.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk))
+        sm = float(clk.value) if rc == 0 else None
+        if self.power_source == "instant":
+            pw = self._power_instant()
+        else:
+            pw = mw.value / 1000.0 if self.L.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw)) == 0 else None
+        rs = reasons.value if self.L.nvmlDeviceGetCurrentClocksEventReasons(self.h, ct.byref(reasons)) == 0 else 0
+        self.samples.append((t, sm, pw, rs, (time.perf_counter() - t) * 1e6))
+
+    def _run(self):
+        while not self.stop_ev.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def stop(self):
+        self.stop_ev.set()
+        self.thread.join(timeout=5)
+        try:
+            self.L.nvmlShutdown()
+        except Exception:
+            pass
+
+    def summary(self, t0: float, t1: float) -> dict:
+        use = [x for x in self.samples if t0 <= x[0] <= t1 and x[1] is not None]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": self.sm_max, "reasons": [], "samples": 0,
+                    "source": "nvml", "in_timed_region": False}
+        reasons = set()
+        for x in use:
+            for bit, nm in self.REASONS.items():
+                if x[3] & bit:
+                    reasons.add(nm)
+        power = [x[2] for x in use if x[2] is not None]
+        return {
+            "sm_mhz": statistics.median(x[1] for x in use),
+            "sm_max_mhz": self.sm_max,
+            "sm_mhz_min": min(x[1] for x in use),
+            "reasons": sorted(reasons),
+            "samples": len(use),
+            "in_timed_region": True,
+            "power_w_median": round(statistics.median(power), 1) if power else None,
+            "power_w_max": round(max(power), 1) if power else None,
+            "power_source": self.power_source,
+            "period_ms": round(1e3 * (use[-1][0] - use[0][0]) / max(1, len(use) - 1), 2),
+            "source": "nvml (in-process polling, query only)",
+        }
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -404,8 +511,28 @@ def measure_e2e(g, ctx, w, host, stream, steps, batches=3):
             "api": "gemm_run_host (pinned host buffers)"}
 
 
-def cpu_baseline(w, host, target_s=12.0, max_rows=None):
-    """The FP64 oracle, as it stands, on a bounded row sample of the workload."""
+# Parity rule of the GEMM path against the FP64 oracle (the one the tests apply): per element
+# |C - ref| <= 1e-2 + 4e-3 |ref|, relative Frobenius error <= 1e-3, no NaN/Inf.
+PARITY_ATOL, PARITY_RTOL, PARITY_FRO = 1e-2, 4e-3, 1e-3
+
+
+def parity_stats(got, ref) -> dict:
+    import numpy as np
+    g = np.asarray(got, dtype=np.float16).astype(np.float64)
+    r = np.asarray(ref, dtype=np.float16).astype(np.float64)
+    err = np.abs(g - r)
+    viol = int((err > PARITY_ATOL + PARITY_RTOL * np.abs(r)).sum())
+    fro = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30))
+    finite = bool(np.all(np.isfinite(g)))
+    return {"checked_elements": int(err.size), "max_abs": float(err.max()), "fro_rel": fro, "violations": viol,
+            "finite": finite, "ok": finite and viol == 0 and fro <= PARITY_FRO,
+            "tolerance": f"|C-ref| <= {PARITY_ATOL} + {PARITY_RTOL}|ref|, fro <= {PARITY_FRO}"}
+
+
+def cpu_baseline(w, host, target_s=12.0, max_rows=None, gpu_out=None):
+    """The FP64 oracle, as it stands, on a bounded row sample of the workload. When the GPU's
+    output of the timed launches (host copy) is given, the same oracle rows check it: the
+    benchmark's own output is verified against the oracle in the same run."""
     import oracle
     from tensor_core_gemm_tcgen05_gb300 import inputs
     A, B, bias = host
@@ -418,14 +545,81 @@ def cpu_baseline(w, host, target_s=12.0, max_rows=None):
     nrows = int(min(max_rows or w.M, max(len(probe_rows), rate * target_s)))
     rows = inputs.sample_rows(w.M, nrows, include_last=min(w.include_last, nrows)).numpy()
     t0 = time.perf_counter()
-    _, _, used = oracle.gemm(A, B, bias, w.epi_code, rows=rows)
+    ref, _, used = oracle.gemm(A, B, bias, w.epi_code, rows=rows)
     dt = time.perf_counter() - t0
     flops = 2.0 * len(rows) * w.N * w.K
-    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": used, "kind": "oracle",
-            "seconds": round(dt, 3),
-            "sample": f"{len(rows)} seeded full rows of C ({len(rows)} x {w.N}, K={w.K}, "
-                      f"{w.epilogue} epilogue) out of M={w.M}, FP64 C oracle, {used} threads",
-            "extrapolated_full_gemm_s": round(dt * w.M / len(rows), 1)}
+    res = {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+           "seconds": round(dt, 3),
+           "sample": f"{len(rows)} seeded full rows of C ({len(rows)} x {w.N}, K={w.K}, "
+                     f"{w.epilogue} epilogue) out of M={w.M}, FP64 C oracle, {used} threads",
+           "extrapolated_full_gemm_s": round(dt * w.M / len(rows), 1)}
+    parity = None
+    if gpu_out is not None:
+        parity = parity_stats(gpu_out[rows], ref)
+        parity["rows"] = f"the {len(rows)} oracle rows above (including the last {min(w.include_last, nrows)})"
+        parity["of"] = "C of the timed launches"
+    return res, parity
+
+
+def start_clock_probe(g, ctx, device, region_ms, interval_us=100.0, max_samples=32768):
+    """Start the library's SM-clock sampler on a stream of its own, for about `region_ms`
+    (plus a margin): one thread beside the timed kernels reads the SM cycle counter and the
+    global timer every `interval_us`."""
+    import torch
+    n = int(min(max_samples, region_ms * 1.3 * 1e3 / interval_us + 64))
+    trace = torch.zeros(2 * n, dtype=torch.int64, device=device)
+    side = torch.cuda.Stream(device)
+    g.gemm_clock_trace(ctx, trace, n, int(interval_us * 1e3), int((region_ms * 1.3 + 1.0) * 1e6), side)
+    return trace
+
+
+def clock_probe_summary(trace, region_ms) -> dict:
+    """SM clock over the first `region_ms` of the trace (the timed launches start right after
+    the sampler): cycles / ns between consecutive samples."""
+    import numpy as np
+    t = trace.view(-1, 2).cpu().numpy()
+    t = t[t[:, 0] > 0]
+    if len(t) < 3:
+        return {"samples": int(len(t))}
+    ts, cs = t[:, 0].astype(np.float64), t[:, 1].astype(np.float64)
+    end = ts[0] + region_ms * 1e6
+    ok = ts[1:] <= end
+    mhz = (np.diff(cs) / np.diff(ts) * 1e3)[ok]
+    if len(mhz) == 0:
+        return {"samples": int(len(t))}
+    return {"effective_sm_mhz": round(float(np.median(mhz)), 1), "effective_sm_mhz_min": round(float(mhz.min()), 1),
+            "effective_sm_mhz_max": round(float(mhz.max()), 1), "intervals": int(len(mhz)),
+            "interval_us": round(float(np.median(np.diff(ts))) / 1e3, 1),
+            "source": "gemm_clock_trace: clock64 / globaltimer on one SM beside the timed launches"}
+
+
+def time_sustained(g, ctx, w, bufs, stream, step_ms, sampler, seconds=2.0):
+    """The same launches back to back for about `seconds` (at least 1.5 s), right after the
+    headline: the steady state at the board's power limit, with its own clock record."""
+    import torch
+    dA, dB, dbias, dC = bufs
+    n = max(50, int(math.ceil(seconds * 1e3 / max(step_ms, 1e-3))))
+    torch.cuda.synchronize()
+    trace = start_clock_probe(g, ctx, dA.device, n * step_ms, interval_us=1000.0)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(n):
+        g.gemm_run(ctx, w.M, w.N, w.K, dA, dB, dbias, dC, w.epi_code, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    ms = e0.elapsed_time(e1)
+    clocks = sampler.summary(t0, t1) if sampler else None
+    # the last half alone: after the clocks have settled at the power limit
+    clocks_late = sampler.summary(t0 + 0.5 * (t1 - t0), t1) if sampler else None
+    probe = clock_probe_summary(trace, ms)
+    if clocks is not None:
+        clocks.update(probe)
+    else:
+        clocks = probe
+    return n, ms, clocks, clocks_late
 
 
 def run_ours(args):
@@ -445,32 +639,48 @@ def run_ours(args):
     w = inputs.WORKLOADS[args.workload]
     host, (dA, dB, dbias, dC) = device_buffers(w, device)
     peaks, peak_src = load_peaks()
+    schedule = g.gemm_describe(ctx, w.M, w.N, w.K, w.epi_code)
 
-    sampler = ClockSampler(local) if rank == 0 else None
-    # warm-up, then the timed region (clock samples are kept only inside it)
+    sampler = None
+    sampler_note = None
+    if rank == 0:
+        try:
+            sampler = NvmlSampler(local)
+        except Exception as e:   # no NVML: fall back to nvidia-smi at 100 ms
+            sampler_note = f"NVML unavailable ({e}); nvidia-smi sampling"
+    smi = ClockSampler(local) if rank == 0 and sampler is None else None
+    # warm-up (its duration sizes the clock sampler), then the timed region (clock samples
+    # are kept only inside it)
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
     for _ in range(args.warmup):
         g.gemm_run(ctx, w.M, w.N, w.K, dA, dB, dbias, dC, w.epi_code, stream)
+    w1.record(stream)
     torch.cuda.synchronize()
+    est_region_ms = w0.elapsed_time(w1) / args.warmup * args.steps
     barrier(dist, device)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    if sampler:
-        sampler.mark_start()
+    trace = start_clock_probe(g, ctx, device, est_region_ms) if rank == 0 else None
+    if smi:
+        smi.mark_start()
+    t_start = time.perf_counter()
     e0.record(stream)
     for _ in range(args.steps):
         g.gemm_run(ctx, w.M, w.N, w.K, dA, dB, dbias, dC, w.epi_code, stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    if sampler:
-        sampler.mark_stop()
+    t_stop = time.perf_counter()
+    if smi:
+        smi.mark_stop()
     ms_local = e0.elapsed_time(e1)
     barrier(dist, device)
     ms = max_over_ranks(dist, ms_local, device)
     status, detail = g.gemm_last_device_error(ctx)
     if status != g.GEMM_OK:
         raise RuntimeError(f"device error word {detail} during the timed region")
-    clocks = sampler.finish() if sampler else None
     launches = args.steps  # one kernel launch per step
 
     ms_step = ms / args.steps
@@ -480,6 +690,35 @@ def run_ours(args):
         if dist:
             dist.destroy_process_group()
         return
+    if sampler:
+        clocks = sampler.summary(t_start, t_stop)
+        clocks["note"] = ("NVML's clock and power readings refresh more slowly than a region of a "
+                          "few tens of milliseconds; effective_sm_mhz is the clock the SMs counted")
+    else:
+        clocks = smi.finish()
+        clocks["note"] = sampler_note
+    clocks.update(clock_probe_summary(trace, ms_local))
+    mhz = clocks.get("effective_sm_mhz") or clocks.get("sm_mhz")
+    if mhz:
+        # cycles of one launch at the clock measured inside the timed region
+        clocks["cycles_per_launch"] = round(ms_step * 1e-3 * mhz * 1e6)
+    c_out = dC.cpu().numpy() if not args.no_cpu_baseline and world == 1 else None   # outputs of the timed launches
+
+    sustained = None
+    if not args.no_sustained:
+        n_s, ms_s, clk_s, clk_late = time_sustained(g, ctx, w, (dA, dB, dbias, dC), stream, ms_step, sampler)
+        v_s = w.flops * n_s / (ms_s * 1e-3) / 1e12
+        peak_s = float(peaks["bf16_tflops_sustained"])
+        sustained = {"value": round(v_s, 2), "unit": "TFLOP/s", "launches": n_s, "seconds": round(ms_s * 1e-3, 3),
+                     "ms_per_launch": round(ms_s / n_s, 5), "peak": peak_s,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (FP16 = BF16 nominal rate)",
+                     "frac": round(v_s / peak_s, 4), "clocks": clk_s, "clocks_last_half": clk_late}
+        mhz_s = clk_s and (clk_s.get("effective_sm_mhz") or clk_s.get("sm_mhz"))
+        if mhz_s:
+            sustained["cycles_per_launch"] = round(ms_s / n_s * 1e-3 * mhz_s * 1e6)
+        status, detail = g.gemm_last_device_error(ctx)
+        if status != g.GEMM_OK:
+            raise RuntimeError(f"device error word {detail} during the sustained run")
 
     long_region = ms >= 1000.0
     peak_key = "bf16_tflops_sustained" if long_region else "bf16_tflops"
@@ -491,7 +730,7 @@ def run_ours(args):
         "frac": round(per_gpu / peak, 4), "traffic": traffic,
         "peak_source": f"{peak_src} {peak_key} (FP16 = BF16 nominal rate)",
         "traffic_source": traffic_src, "algorithmic_flops_per_launch": w.flops,
-        "algorithmic_bytes_per_launch": w.bytes, "kernel": "gemm_tcgen05_pair_kernel (CTA pairs, 256x256 tiles)",
+        "algorithmic_bytes_per_launch": w.bytes, "kernel": schedule.split(" ")[0], "schedule": schedule,
     }
 
     side = {}
@@ -505,7 +744,8 @@ def run_ours(args):
             t = time_device(g, ctx, sw, a, b, bi, c, stream, n, 5)
             tf = sw.flops / (t / n * 1e-3) / 1e12
             side[name] = {"tflops": round(tf, 2), "us_per_launch": round(t / n * 1e3, 2),
-                          "pct_of_burst_peak": round(100 * tf / float(peaks["bf16_tflops"]), 2)}
+                          "pct_of_burst_peak": round(100 * tf / float(peaks["bf16_tflops"]), 2),
+                          "kernel": g.gemm_describe(ctx, sw.M, sw.N, sw.K, sw.epi_code)}
             del a, b, bi, c
         torch.cuda.empty_cache()
         side.update(measure_cublas_context(device, peaks))
@@ -514,8 +754,12 @@ def run_ours(args):
         side.update(measure_attention(g, ctx, stream, device, peaks))
 
     e2e = None if args.no_e2e else measure_e2e(g, ctx, w, host, stream, steps=max(3, min(args.steps, 10)))
-    base = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, host)
+    base, parity = (None, None)
+    if not args.no_cpu_baseline and world == 1:
+        base, parity = cpu_baseline(w, host, gpu_out=c_out)
     ctx.close()
+    if sampler:
+        sampler.stop()
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -529,14 +773,19 @@ def run_ours(args):
         "pct_of_peak": round(100 * per_gpu / float(peaks["bf16_tflops"]), 2),
         "roofline": roofline,
         "cpu_baseline": base,
+        "parity": parity,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
+        "sustained": sustained,
         "side_workloads": side,
     }
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+    if parity is not None and not parity["ok"]:
+        log(f"parity check of the benchmark's output FAILED: {parity}")
+        sys.exit(1)
 
 
 # ---------------------------------------------------------------------------------------------
@@ -596,6 +845,7 @@ def main(argv=None):
     ap.add_argument("--no-side", action="store_true", help="skip the context workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--no-sustained", action="store_true", help="skip the seconds-long sustained leg")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -153,6 +153,35 @@ const char *gemm_status_string(int status);
 /* Number of streaming multiprocessors the one-CTA kernel sizes its grid to. */
 int gemm_num_sms(gemm_ctx *ctx);
 
+/* Which kernel instance gemm_run would launch for an M x N x K problem with `epilogue`, with
+ * the context's current debug flags: writes a NUL-terminated description of at most len - 1
+ * characters to `buf` (host memory owned by the caller), of the form
+ *   "<kernel instance> grid=<CTAs> cluster=<CTAs per cluster> tiles=<output tiles>",
+ * e.g. "gemm_tcgen05_pair_kernel<PairConfig<256,6,4>> grid=148 cluster=2 tiles=2112".
+ * The kernel instance names the template instance as it appears in a profiler's kernel
+ * list. Launches nothing and touches no device memory. Returns GEMM_OK, or the status
+ * gemm_run would return for these sizes and epilogue (GEMM_ERR_ARG, GEMM_ERR_ALIGN), or
+ * GEMM_ERR_ARG for a NULL `buf` or len <= 0. (No counterpart in the tutorial pages: it
+ * reports the schedule choice so that measurements can name the kernel they time.) */
+int gemm_describe(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, int epilogue, char *buf, int64_t len);
+
+/* Measurement aid (no counterpart in the tutorial pages): samples the SM clock while other
+ * work runs. One thread of a 32-thread CTA (no shared memory) reads the global nanosecond
+ * timer and the SM cycle counter every `interval_ns` and writes trace[2i] = timer (ns),
+ * trace[2i + 1] = cycles, for i < max_samples, until `duration_ns` has passed since its first
+ * sample; it sleeps in between. Launched on `stream`, asynchronous: put it on a stream of its
+ * own just before the kernels to be timed, and it runs beside them on one SM (one warp
+ * slot); (cycles difference) / (timer difference) of consecutive samples is the SM clock in
+ * GHz over that interval.
+ *   trace: device memory of the context's device, 2 * max_samples uint64, 16-byte aligned,
+ *          owned by the caller; entries past the last sample are not written (zero-fill it
+ *          first to find the count).
+ *   1 <= max_samples <= 2^20, 1000 <= interval_ns <= 1e7, duration_ns <= 1e10.
+ * Returns GEMM_OK once launched, GEMM_ERR_ARG / _ALIGN / _DEVICE before launching, or
+ * GEMM_ERR_LAUNCH. */
+int gemm_clock_trace(gemm_ctx *ctx, uint64_t *trace, int max_samples, uint64_t interval_ns,
+                     uint64_t duration_ns, void *stream);
+
 /* Number of CTA pairs (2-SM clusters) the device can run at once with the pair kernel,
  * which takes 256 x 256 tiles; 0 if the pair kernel cannot run (then every call uses the
  * one-CTA kernel). gemm_run picks the pair kernel when the problem has at least this many

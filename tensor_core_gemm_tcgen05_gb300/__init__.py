@@ -44,7 +44,7 @@ EXPORTS = (
     "gemm_create", "gemm_run", "gemm_run_host", "gemm_last_device_error",
     "gemm_last_cuda_error", "gemm_destroy", "gemm_status_string", "gemm_num_sms",
     "gemm_set_timeout_ns", "gemm_set_debug", "gemm_run_noalloc", "gemm_num_pairs",
-    "gemm_row_softmax", "gemm_attention_fwd",
+    "gemm_row_softmax", "gemm_attention_fwd", "gemm_describe", "gemm_clock_trace",
 )
 GEMM_NOALLOC_SCRATCH_BYTES = 256
 
@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
             L.gemm_set_timeout_ns.argtypes = [vp, ctypes.c_uint64]
             L.gemm_set_debug.argtypes = [vp, i32]
             L.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, i32, vp]
+            L.gemm_describe.argtypes = [vp, i64, i64, i64, i32, ctypes.c_char_p, i64]
+            L.gemm_clock_trace.argtypes = [vp, vp, i32, ctypes.c_uint64, ctypes.c_uint64, vp]
             for name in EXPORTS:
                 if name != "gemm_status_string":
                     getattr(L, name).restype = i32
@@ -205,6 +207,20 @@ def gemm_num_sms(ctx) -> int:
 
 def gemm_num_pairs(ctx) -> int:
     return int(lib().gemm_num_pairs(_h(ctx)))
+
+
+def gemm_describe(ctx, M, N, K, epilogue=EPI_NONE) -> str:
+    """The kernel instance, grid, cluster size and tile count gemm_run would use."""
+    buf = ctypes.create_string_buffer(256)
+    _check(lib().gemm_describe(_h(ctx), M, N, K, int(epilogue), buf, len(buf)), "gemm_describe")
+    return buf.value.decode()
+
+
+def gemm_clock_trace(ctx, trace, max_samples, interval_ns, duration_ns, stream=None) -> int:
+    """Launch the SM-clock sampler into ``trace`` (device, 2 * max_samples int64/uint64)."""
+    rc = lib().gemm_clock_trace(_h(ctx), _ptr(trace), int(max_samples), int(interval_ns), int(duration_ns),
+                                _stream(stream, _dev(ctx)))
+    return _check(rc, "gemm_clock_trace")
 
 
 def gemm_row_softmax(ctx, rows, cols, X, Y, stream=None) -> int:

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <new>
 
@@ -14,6 +15,7 @@
 #include "gemm_kernel_pair.cuh"
 #include "softmax_kernel.cuh"
 #include "attention_kernel.cuh"
+#include "clock_probe.cuh"
 
 namespace {
 
@@ -154,9 +156,8 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
     return a0 < b0 + nb && b0 < a0 + na;
 }
 
-// Shape/pointer rules shared by gemm_run and gemm_run_host (everything but memory kind).
-int check_args(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, const void *B,
-               const void *bias, void *C, int epilogue)
+// Size and epilogue rules (no pointers): GEMM_OK also for the empty problems M = 0 or N = 0.
+int check_shape(const gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, int epilogue)
 {
     if (!ctx)
         return GEMM_ERR_ARG;
@@ -166,8 +167,6 @@ int check_args(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, co
         return GEMM_ERR_ARG;
     if (M == 0 || N == 0)
         return GEMM_OK;
-    if (!C || (K > 0 && (!A || !B)))
-        return GEMM_ERR_ARG;
     if (epilogue == GEMM_EPI_SOFTMAX) {
         // a row takes a cluster of ceil(N / 256) CTAs
         const int64_t cs = (N + kSoftmaxTileN - 1) / kSoftmaxTileN;
@@ -176,6 +175,18 @@ int check_args(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, co
     }
     if (N % 8 != 0 || K % 8 != 0)
         return GEMM_ERR_ALIGN;
+    return GEMM_OK;
+}
+
+// Shape/pointer rules shared by gemm_run and gemm_run_host (everything but memory kind).
+int check_args(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+               const void *bias, void *C, int epilogue)
+{
+    int rc = check_shape(ctx, M, N, K, epilogue);
+    if (rc != GEMM_OK || M == 0 || N == 0)
+        return rc;
+    if (!C || (K > 0 && (!A || !B)))
+        return GEMM_ERR_ARG;
     if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B))) || (bias && !aligned16(bias)))
         return GEMM_ERR_ALIGN;
     const size_t cb = static_cast<size_t>(M) * N * 2;
@@ -244,6 +255,119 @@ void launch_pdl_cluster(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, gb
     cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p);
 }
 
+// The kernel instance gemm_run launches for a problem, with its grid and the schedule fields
+// of its parameters. make_plan decides; launch runs the plan; gemm_describe reports it.
+enum PlanKind : int { PLAN_PAIR, PLAN_TILES, PLAN_TILES8, PLAN_STREAMK, PLAN_SPLITK, PLAN_ROWCLUSTER };
+
+struct Plan {
+    PlanKind kind = PLAN_TILES;
+    int grid = 0;      // CTAs launched
+    int cluster = 1;   // CTAs per thread-block cluster (1: no cluster attribute)
+    int m_blocks = 0, n_blocks = 0, num_tiles = 0, group_m = 1;
+    int split = 0, row_cluster = 0;
+    int64_t sk_units = 0;
+};
+
+const char *plan_kernel_name(PlanKind k)
+{
+    switch (k) {
+    case PLAN_PAIR: return "gemm_tcgen05_pair_kernel<PairConfig<256,6,4>>";
+    case PLAN_TILES: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_TILES>";
+    case PLAN_TILES8: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,8>,SCHED_TILES>";
+    case PLAN_STREAMK: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_STREAM_K>";
+    case PLAN_SPLITK: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,8>,SCHED_SPLIT_K>";
+    case PLAN_ROWCLUSTER: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,8>,SCHED_ROW_CLUSTER>";
+    }
+    return "unknown";
+}
+
+// Choose the kernel instance and grid for an M x N x K problem (sizes already checked,
+// M, N > 0).
+Plan make_plan(const gemm_ctx *ctx, int M, int N, int K, int epilogue)
+{
+    Plan pl;
+    const int num_kb = (K + Cfg::BK - 1) / Cfg::BK;
+    if (epilogue == GEMM_EPI_SOFTMAX) {
+        // one cluster of n_blocks CTAs (a single CTA when N <= 256) per 128-row block
+        static_assert(Cfg8::BM == Cfg::BM && Cfg8::BN == Cfg::BN && Cfg8::BK == Cfg::BK &&
+                          Cfg8::B_BOX_N == Cfg::B_BOX_N,
+                      "same tensor-map boxes as the GEMM kernel");
+        pl.kind = PLAN_ROWCLUSTER;
+        pl.m_blocks = (M + Cfg8::BM - 1) / Cfg8::BM;
+        pl.n_blocks = (N + Cfg8::BN - 1) / Cfg8::BN;
+        pl.num_tiles = pl.m_blocks * pl.n_blocks;
+        pl.group_m = 1;
+        pl.row_cluster = pl.n_blocks;
+        pl.cluster = pl.n_blocks;
+        pl.grid = std::min(pl.m_blocks, ctx->row_clusters[pl.n_blocks]) * pl.n_blocks;
+        return pl;
+    }
+    // 256 x 256 tiles on CTA pairs when there are enough of them to give every pair at
+    // least one; otherwise 128 x 256 tiles on single SMs (twice as many tiles to spread).
+    const int pair_tiles = ((M + PairCfg::BM - 1) / PairCfg::BM) * ((N + PairCfg::BN - 1) / PairCfg::BN);
+    bool pair = ctx->max_clusters > 0 && pair_tiles >= ctx->max_clusters;
+    if (ctx->debug & (GEMM_DEBUG_FORCE_SINGLE | GEMM_DEBUG_FORCE_SPLITK))
+        pair = false;
+    if ((ctx->debug & GEMM_DEBUG_FORCE_PAIR) && ctx->max_clusters > 0)
+        pair = true;
+    if (pair) {
+        pl.kind = PLAN_PAIR;
+        pl.m_blocks = (M + PairCfg::BM - 1) / PairCfg::BM;
+        pl.n_blocks = (N + PairCfg::BN - 1) / PairCfg::BN;
+        pl.num_tiles = pl.m_blocks * pl.n_blocks;
+        pl.group_m = raster_group(pl.m_blocks, PairCfg::BM, K);
+        pl.cluster = 2;
+        pl.grid = 2 * std::min(pl.num_tiles, ctx->max_clusters);
+        return pl;
+    }
+    pl.m_blocks = (M + Cfg::BM - 1) / Cfg::BM;
+    pl.n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
+    pl.num_tiles = pl.m_blocks * pl.n_blocks;
+    pl.group_m = raster_group(pl.m_blocks, Cfg::BM, K);
+    pl.grid = std::min(pl.num_tiles, ctx->num_sms);
+    // Split-K when the tiles leave most SMs idle: a cluster of S CTAs per tile, each with
+    // 1/S of the k-blocks (at least kSplitKMinBlocks of them), the partials summed over
+    // DSMEM; S = 8, 4 or 2, the largest whose clusters all run at once.
+    const int64_t units = static_cast<int64_t>(pl.num_tiles) * num_kb;
+    int split = 0;
+    if (units > 0 && !(ctx->debug & GEMM_DEBUG_FORCE_STREAMK)) {
+        for (int cs = 8; cs >= 2 && !split; cs /= 2) {
+            if (ctx->split_clusters[cs] <= 0 || num_kb < cs)
+                continue;
+            if (ctx->debug & GEMM_DEBUG_FORCE_SPLITK)
+                split = cs;   // any tile count (several waves) and any k-blocks >= cs
+            else if (static_cast<int64_t>(pl.num_tiles) * cs <= ctx->num_sms &&
+                     pl.num_tiles <= ctx->split_clusters[cs] && num_kb >= kSplitKMinBlocks * cs)
+                split = cs;
+        }
+    }
+    if (split > 0) {
+        pl.kind = PLAN_SPLITK;
+        pl.split = split;
+        pl.cluster = split;
+        pl.grid = pl.num_tiles * split;
+        return pl;
+    }
+    // Otherwise stream-K when the tiles leave most SMs idle: the (tile, k-block) units are
+    // split evenly over up to every SM.
+    if (units > 0) {
+        int g_sk = 0;
+        if (ctx->debug & GEMM_DEBUG_FORCE_STREAMK)
+            g_sk = static_cast<int>(std::min<int64_t>(ctx->num_sms, units));
+        else if (static_cast<int64_t>(pl.num_tiles) * kStreamKMinSpread <= ctx->num_sms)
+            g_sk = static_cast<int>(std::min<int64_t>(ctx->num_sms, units / kStreamKMinUnits));
+        if (g_sk >= kStreamKMinSpread * pl.num_tiles || ((ctx->debug & GEMM_DEBUG_FORCE_STREAMK) && g_sk > 0)) {
+            pl.kind = PLAN_STREAMK;
+            pl.sk_units = units;
+            pl.grid = g_sk;
+            return pl;
+        }
+    }
+    // one wave: eight epilogue warps
+    pl.kind = pl.num_tiles <= ctx->num_sms ? PLAN_TILES8 : PLAN_TILES;
+    return pl;
+}
+
 // ldb / ldc: row strides of B and C in elements (0: N, tightly packed); A is always packed.
 // gemm_run_host uses them to run column bands of a larger B and C.
 int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, const void *bias, void *C,
@@ -262,6 +386,7 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     if (!encode_2d(ctx, &tc, C, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 32, 32,
                    CU_TENSOR_MAP_SWIZZLE_64B, static_cast<uint64_t>(ldc)))
         return GEMM_ERR_LAUNCH;
+    const Plan pl = make_plan(ctx, M, N, K, epilogue);
     gb300::GemmParams p;
     p.M = M;
     p.N = N;
@@ -274,95 +399,42 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     p.err = ctx->d_err;
     p.timeout_ns = ctx->timeout_ns;
     p.debug = ctx->debug & GEMM_DEBUG_WITHHOLD_FIRST_LOAD;
-    // 256 x 256 tiles on CTA pairs when there are enough of them to give every pair at
-    // least one; otherwise 128 x 256 tiles on single SMs (twice as many tiles to spread).
-    if (epilogue == GEMM_EPI_SOFTMAX) {
-        // one cluster of n_blocks CTAs (a single CTA when N <= 256) per 128-row block
-        static_assert(Cfg8::BM == Cfg::BM && Cfg8::BN == Cfg::BN && Cfg8::BK == Cfg::BK &&
-                          Cfg8::B_BOX_N == Cfg::B_BOX_N,
-                      "same tensor-map boxes as the GEMM kernel");
-        p.m_blocks = (M + Cfg8::BM - 1) / Cfg8::BM;
-        p.n_blocks = (N + Cfg8::BN - 1) / Cfg8::BN;
-        p.num_tiles = p.m_blocks * p.n_blocks;
-        p.group_m = 1;
-        p.row_cluster = p.n_blocks;
-        const int clusters = std::min(p.m_blocks, ctx->row_clusters[p.n_blocks]);
-        launch_pdl_cluster(gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_ROW_CLUSTER>, clusters * p.n_blocks,
-                           p.n_blocks, Cfg8::NUM_THREADS, Cfg8::SMEM_BYTES, stream, ta, tb, tc, p);
-        const cudaError_t e = cudaGetLastError();
-        return e == cudaSuccess ? GEMM_OK : cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+    p.m_blocks = pl.m_blocks;
+    p.n_blocks = pl.n_blocks;
+    p.num_tiles = pl.num_tiles;
+    p.group_m = pl.group_m;
+    p.split = pl.split;
+    p.row_cluster = pl.row_cluster;
+    if (pl.kind == PLAN_STREAMK) {
+        p.sk_units = pl.sk_units;
+        p.sk_ws = ctx->sk_ws;
+        p.sk_flags = ctx->sk_flags;
     }
-    const int pair_tiles = ((M + PairCfg::BM - 1) / PairCfg::BM) * ((N + PairCfg::BN - 1) / PairCfg::BN);
-    bool pair = ctx->max_clusters > 0 && pair_tiles >= ctx->max_clusters;
-    if (ctx->debug & (GEMM_DEBUG_FORCE_SINGLE | GEMM_DEBUG_FORCE_SPLITK))
-        pair = false;
-    if ((ctx->debug & GEMM_DEBUG_FORCE_PAIR) && ctx->max_clusters > 0)
-        pair = true;
-    if (pair) {
-        p.m_blocks = (M + PairCfg::BM - 1) / PairCfg::BM;
-        p.n_blocks = (N + PairCfg::BN - 1) / PairCfg::BN;
-        p.num_tiles = p.m_blocks * p.n_blocks;
-        p.group_m = raster_group(p.m_blocks, PairCfg::BM, K);
-        const int grid = 2 * std::min(p.num_tiles, ctx->max_clusters);
-        launch_pdl(gb300::gemm_tcgen05_pair_kernel<PairCfg>, grid, PairCfg::NUM_THREADS, PairCfg::SMEM_BYTES, stream,
-                   ta, tb, tc, p);
-    } else {
-        p.m_blocks = (M + Cfg::BM - 1) / Cfg::BM;
-        p.n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
-        p.num_tiles = p.m_blocks * p.n_blocks;
-        p.group_m = raster_group(p.m_blocks, Cfg::BM, K);
-        int grid = std::min(p.num_tiles, ctx->num_sms);
-        // Split-K when the tiles leave most SMs idle: a cluster of S CTAs per tile, each with
-        // 1/S of the k-blocks (at least kSplitKMinBlocks of them), the partials summed over
-        // DSMEM; S = 8, 4 or 2, the largest whose clusters all run at once. (The fused softmax
-        // needs whole rows in one CTA: never.)
-        const int64_t units = static_cast<int64_t>(p.num_tiles) * p.num_kb;
-        int split = 0;
-        if (epilogue != GEMM_EPI_SOFTMAX && units > 0 && !(ctx->debug & GEMM_DEBUG_FORCE_STREAMK)) {
-            for (int cs = 8; cs >= 2 && !split; cs /= 2) {
-                if (ctx->split_clusters[cs] <= 0 || p.num_kb < cs)
-                    continue;
-                if (ctx->debug & GEMM_DEBUG_FORCE_SPLITK)
-                    split = cs;   // any tile count (several waves) and any k-blocks >= cs
-                else if (static_cast<int64_t>(p.num_tiles) * cs <= ctx->num_sms &&
-                         p.num_tiles <= ctx->split_clusters[cs] && p.num_kb >= kSplitKMinBlocks * cs)
-                    split = cs;
-            }
-        }
-        if (split > 0) {
-            p.split = split;
-            launch_pdl_cluster(gb300::gemm_tcgen05_kernel<SplitCfg, gb300::SCHED_SPLIT_K>, p.num_tiles * split, split,
-                               SplitCfg::NUM_THREADS, SplitCfg::SMEM_BYTES, stream, ta, tb, tc, p);
-            const cudaError_t e = cudaGetLastError();
-            return e == cudaSuccess ? GEMM_OK : cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
-        }
-        // Otherwise stream-K when the tiles leave most SMs idle: the (tile, k-block) units are
-        // split evenly over up to every SM.
-        if (epilogue != GEMM_EPI_SOFTMAX && units > 0) {
-            int g_sk = 0;
-            if (ctx->debug & GEMM_DEBUG_FORCE_STREAMK)
-                g_sk = static_cast<int>(std::min<int64_t>(ctx->num_sms, units));
-            else if (static_cast<int64_t>(p.num_tiles) * kStreamKMinSpread <= ctx->num_sms)
-                g_sk = static_cast<int>(std::min<int64_t>(ctx->num_sms, units / kStreamKMinUnits));
-            if (g_sk >= kStreamKMinSpread * p.num_tiles || ((ctx->debug & GEMM_DEBUG_FORCE_STREAMK) && g_sk > 0)) {
-                p.sk_units = units;
-                p.sk_ws = ctx->sk_ws;
-                p.sk_flags = ctx->sk_flags;
-                grid = g_sk;
-            }
-        }
-        static_assert(Cfg8::BM == Cfg::BM && Cfg8::BN == Cfg::BN && Cfg8::BK == Cfg::BK &&
-                          Cfg8::B_BOX_N == Cfg::B_BOX_N,
-                      "same tensor-map boxes");
-        if (p.sk_units > 0)
-            launch_pdl(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_STREAM_K>, grid, Cfg::NUM_THREADS,
-                       Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
-        else if (p.num_tiles <= ctx->num_sms)   // one wave: eight epilogue warps
-            launch_pdl(gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_TILES>, grid, Cfg8::NUM_THREADS,
-                       Cfg8::SMEM_BYTES, stream, ta, tb, tc, p);
-        else
-            launch_pdl(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_TILES>, grid, Cfg::NUM_THREADS,
-                       Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
+    switch (pl.kind) {
+    case PLAN_ROWCLUSTER:
+        launch_pdl_cluster(gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_ROW_CLUSTER>, pl.grid, pl.cluster,
+                           Cfg8::NUM_THREADS, Cfg8::SMEM_BYTES, stream, ta, tb, tc, p);
+        break;
+    case PLAN_PAIR:
+        launch_pdl(gb300::gemm_tcgen05_pair_kernel<PairCfg>, pl.grid, PairCfg::NUM_THREADS, PairCfg::SMEM_BYTES,
+                   stream, ta, tb, tc, p);
+        break;
+    case PLAN_SPLITK:
+        launch_pdl_cluster(gb300::gemm_tcgen05_kernel<SplitCfg, gb300::SCHED_SPLIT_K>, pl.grid, pl.cluster,
+                           SplitCfg::NUM_THREADS, SplitCfg::SMEM_BYTES, stream, ta, tb, tc, p);
+        break;
+    case PLAN_STREAMK:
+        launch_pdl(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_STREAM_K>, pl.grid, Cfg::NUM_THREADS,
+                   Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
+        break;
+    case PLAN_TILES8:
+        launch_pdl(gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_TILES>, pl.grid, Cfg8::NUM_THREADS,
+                   Cfg8::SMEM_BYTES, stream, ta, tb, tc, p);
+        break;
+    case PLAN_TILES:
+        launch_pdl(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_TILES>, pl.grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES,
+                   stream, ta, tb, tc, p);
+        break;
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -772,7 +844,42 @@ const char *gemm_status_string(int status)
 
 int gemm_num_sms(gemm_ctx *ctx) { return ctx ? ctx->num_sms : 0; }
 
+int gemm_describe(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, int epilogue, char *buf, int64_t len)
+{
+    if (!buf || len <= 0)
+        return GEMM_ERR_ARG;
+    buf[0] = '\0';
+    const int rc = check_shape(ctx, M, N, K, epilogue);
+    if (rc != GEMM_OK)
+        return rc;
+    if (M == 0 || N == 0) {
+        std::snprintf(buf, static_cast<size_t>(len), "none (empty problem, nothing is launched)");
+        return GEMM_OK;
+    }
+    const Plan pl = make_plan(ctx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), epilogue);
+    std::snprintf(buf, static_cast<size_t>(len), "%s grid=%d cluster=%d tiles=%d", plan_kernel_name(pl.kind),
+                  pl.grid, pl.cluster, pl.num_tiles);
+    return GEMM_OK;
+}
+
 int gemm_num_pairs(gemm_ctx *ctx) { return ctx ? ctx->max_clusters : 0; }
+
+int gemm_clock_trace(gemm_ctx *ctx, uint64_t *trace, int max_samples, uint64_t interval_ns, uint64_t duration_ns,
+                     void *stream)
+{
+    if (!ctx || !trace || max_samples < 1 || max_samples > (1 << 20) || interval_ns < 1000u ||
+        interval_ns > 10000000u || duration_ns > 10000000000ull)
+        return GEMM_ERR_ARG;
+    if (!aligned16(trace))
+        return GEMM_ERR_ALIGN;
+    if (!on_device(trace, ctx->device))
+        return GEMM_ERR_DEVICE;
+    DeviceGuard guard(ctx->device);
+    gb300::clock_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(trace, max_samples, interval_ns,
+                                                                               duration_ns);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
+}
 
 int gemm_attention_fwd(gemm_ctx *ctx, int64_t heads, int64_t seq_q, int64_t seq_k, int64_t head_dim, const void *Q,
                        const void *K, const void *V, void *O, float scale, int causal, void *stream)

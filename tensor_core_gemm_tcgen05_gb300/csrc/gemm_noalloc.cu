@@ -189,6 +189,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
     p.epilogue = epilogue;
     p.bias = static_cast<const __half *>(bias);
     p.C = static_cast<__half *>(C);
+    p.ldc = N;   // C is tightly packed
     p.err = s.scratch;
     p.timeout_ns = kTimeoutNs;
     p.debug = 0;

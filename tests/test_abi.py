@@ -33,7 +33,7 @@ def header_constants():
 
 def test_exports_match_header(lib):
     funcs = header_functions()
-    assert len(funcs) == 14
+    assert len(funcs) == 16
     assert sorted(g.EXPORTS) == funcs
     out = subprocess.run(["nm", "-D", "--defined-only", g.LIB_PATH], capture_output=True, text=True,
                          check=True).stdout
@@ -75,6 +75,11 @@ def test_null_context_is_rejected(lib):
     assert lib.gemm_row_softmax(None, 4, 8, 16, 16, None) == g.GEMM_ERR_ARG
     assert lib.gemm_attention_fwd(None, 1, 128, 128, 128, 16, 16, 16, 16, 0.1, 0, None) == g.GEMM_ERR_ARG
     assert lib.gemm_create(None, 0) == g.GEMM_ERR_ARG
+    import ctypes
+    buf = ctypes.create_string_buffer(64)
+    assert lib.gemm_describe(None, 8, 8, 8, 0, buf, 64) == g.GEMM_ERR_ARG
+    assert lib.gemm_describe(None, 8, 8, 8, 0, None, 64) == g.GEMM_ERR_ARG
+    assert lib.gemm_clock_trace(None, 16, 8, 100000, 1000000, None) == g.GEMM_ERR_ARG
     # the allocation-free variant rejects bad sizes before touching CUDA
     assert lib.gemm_run_noalloc(-1, 8, 8, 16, 16, None, 16, 0, None) == g.GEMM_ERR_ARG
     assert lib.gemm_run_noalloc(8, 8, 2 ** 31, 16, 16, None, 16, 0, None) == g.GEMM_ERR_ARG

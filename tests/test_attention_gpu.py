@@ -77,6 +77,18 @@ def test_attention_unequal_lengths_non_causal(ctx):
     check(O.reshape(200, D).numpy(), ref, "Sq=100 Sk=300")
 
 
+@pytest.mark.parametrize("Sq,Sk", [(100, 300), (300, 100), (128, 1000), (1000, 128), (257, 513)],
+                         ids=lambda v: str(v))
+def test_attention_unequal_lengths_causal(ctx, Sq, Sk):
+    """Causal with seq_q != seq_k: query i sees keys 0 .. min(i, seq_k - 1), the mask aligned
+    at the first key as the ABI and the oracle define it. With seq_q < seq_k the keys past the
+    last query are never seen; with seq_q > seq_k every query from seq_k on sees all keys."""
+    Q, K, V = qkv(2, Sq, Sk, 7 * Sq + Sk)
+    O = run(ctx, Q, K, V, 0.09, True)
+    ref, _ = oracle.attention(Q, K, V, 0.09, True)
+    check(O.reshape(2 * Sq, D).numpy(), ref, f"causal Sq={Sq} Sk={Sk}")
+
+
 def test_attention_long_sequence_sampled_rows(ctx):
     H, S = 4, 4096
     Q, K, V = qkv(H, S, S, 5)

@@ -348,6 +348,49 @@ def test_bad_arguments_are_rejected_before_launch(ctx):
     assert 0 <= g.gemm_num_pairs(ctx) <= g.gemm_num_sms(ctx) // 2
 
 
+def test_describe_names_the_dispatched_kernel(ctx):
+    """gemm_describe reports the kernel instance gemm_run launches (the bench names the
+    kernel it times with it): CTA pairs for the MLP problem, split-K clusters for few long
+    tiles, row clusters for the wide softmax, nothing for an empty problem; the shape
+    checks are gemm_run's."""
+    d = g.gemm_describe
+    assert d(ctx, 8200, 16384, 4096, g.EPI_GELU).startswith("gemm_tcgen05_pair_kernel<")
+    assert "SCHED_SPLIT_K" in d(ctx, 1024, 1024, 8192, g.EPI_GELU)
+    wide = d(ctx, 32768, 1024, 128, g.EPI_SOFTMAX)
+    assert "SCHED_ROW_CLUSTER" in wide and "cluster=4" in wide
+    assert d(ctx, 0, 8, 8, g.EPI_NONE).startswith("none")
+    with pytest.raises(g.GemmError) as e:
+        d(ctx, 8, 60, 8, g.EPI_NONE)
+    assert e.value.status == g.GEMM_ERR_ALIGN
+    g.gemm_set_debug(ctx, g.GEMM_DEBUG_FORCE_SINGLE | g.GEMM_DEBUG_FORCE_STREAMK)
+    try:
+        assert "SCHED_STREAM_K" in d(ctx, 1024, 1024, 8192, g.EPI_GELU)
+    finally:
+        g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
+
+
+def test_clock_trace_beside_a_gemm(ctx):
+    """The SM-clock sampler on a stream of its own while a GEMM runs on another: timestamps
+    ascend at the requested interval and the cycles per nanosecond are a plausible SM clock
+    (between 0.3 and 2.5 GHz); the GEMM beside it is still correct."""
+    dev = torch.device("cuda:0")
+    n = 200
+    trace = torch.zeros(2 * n, dtype=torch.int64, device=dev)
+    side = torch.cuda.Stream(dev)
+    g.gemm_clock_trace(ctx, trace, n, 50_000, 5_000_000, side)
+    check(ctx, 1000, 1000, 1000, epi=g.EPI_GELU, with_bias=True, seed=21)
+    torch.cuda.synchronize()
+    t = trace.view(-1, 2).cpu().numpy()
+    t = t[t[:, 0] > 0].astype(np.float64)
+    assert 50 <= len(t) <= n
+    dt = np.diff(t[:, 0])
+    assert np.all(dt > 0) and abs(np.median(dt) - 50_000) < 5_000
+    ghz = np.diff(t[:, 1]) / dt
+    assert np.all((ghz > 0.3) & (ghz < 2.5)), ghz
+    with pytest.raises(g.GemmError):
+        g.gemm_clock_trace(ctx, trace, n, 10, 5_000_000, side)   # interval below 1 us
+
+
 @pytest.mark.parametrize("force", ["single", "pair"])
 def test_bounded_wait_reports_timeout_and_context_survives(ctx, force):
     """The producer withholds its first operand load, so the MMA warp's wait runs out:
