@@ -415,7 +415,9 @@ def measure_fused_softmax(g, ctx, stream, device, peaks, steps=30):
     import torch
     from tensor_core_gemm_tcgen05_gb300 import inputs
     res = {}
-    for wname in ("scores_262144x256x128_softmax", "scores_32768x1024x128_softmax"):
+    for wname in ("scores_262144x256x128_softmax", "scores_32768x512x128_softmax", "scores_32768x1024x128_softmax",
+                  "scores_32768x2048x128_softmax", "scores_16384x4096x128_softmax",
+                  "scores_8192x16384x128_softmax"):
         w = inputs.WORKLOADS[wname]
         _, (dA, dB, dbias, dC) = device_buffers(w, device)
 
@@ -442,6 +444,7 @@ def measure_fused_softmax(g, ctx, stream, device, peaks, steps=30):
         gbs = w.bytes / (out["fused"] * 1e-6) / 1e9
         res[w.name] = {
             "us_per_launch": round(out["fused"], 2), "unfused_us": round(out["unfused"], 2),
+            "kernel": g.gemm_describe(ctx, w.M, w.N, w.K, g.EPI_SOFTMAX),
             "GB/s": round(gbs, 1), "bound": "hbm", "frac_of_measured_hbm": round(gbs / float(peaks["hbm_gbs"]), 4),
             "tflops": round(w.flops / (out["fused"] * 1e-6) / 1e12, 1), "algorithmic_bytes_per_launch": w.bytes}
         del dA, dB, dbias, dC

@@ -13,6 +13,7 @@
 #include "gemm.h"
 #include "gemm_kernel.cuh"
 #include "gemm_kernel_pair.cuh"
+#include "softmax_gemm_kernel.cuh"
 #include "softmax_kernel.cuh"
 #include "attention_kernel.cuh"
 #include "clock_probe.cuh"
@@ -28,10 +29,12 @@ using Cfg = gb300::KernelConfig<128, 256, 4, GB300_EPI_WARPS>;
 #endif
 using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS>;
 // The same 128 x 256 tiles with a shorter ring and eight epilogue warps (two per TMEM lane
-// quarter, each with half of the columns): the softmax epilogue's kernel (softmax GEMMs have
-// small K), and the whole-tile kernel when all tiles fit one wave, where every CTA's
-// epilogue is an exposed tail that twice the warps shorten (2048^3: 15.6 -> 15.0 us).
+// quarter, each with half of the columns): the whole-tile kernel when all tiles fit one
+// wave, where every CTA's epilogue is an exposed tail that twice the warps shorten (2048^3:
+// 15.6 -> 15.0 us).
 using Cfg8 = gb300::KernelConfig<128, 256, 3, 8>;
+// The softmax epilogue's kernel: 128 x 256 tiles, 3-stage ring, sixteen epilogue warps.
+using SoftCfg = gb300::SoftmaxConfig<3>;
 // Split-K runs on the eight-warp instance: twice the warps to stage the partial and to
 // read the other CTAs' partials over DSMEM (measured 2-5 % faster than four on 5 of 6
 // few-tile shapes); its 3-stage ring (144 KB) holds the 128 KB partial.
@@ -53,8 +56,7 @@ int raster_group(int m_blocks, int rows_per_block, int K)
 }
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int64_t kSoftmaxMaxCtas = int64_t(1) << 20;   // row softmax grid cap (CTAs loop past it)
-constexpr int kSoftmaxTileN = 256;    // columns of C per CTA of a softmax row cluster
-constexpr int kRowClusterMax = 16;    // clusters of up to 16 CTAs (N <= 4096)
+constexpr int kSoftmaxClusterMax = 8;   // softmax: clusters of 1, 2, 4 or 8 CTAs per row block
 // gemm_run_host splits C into at most this many bands (column bands: also two row halves of
 // A when A is at least kHostChunkMinBytes) whose uploads, GEMMs and downloads overlap;
 // outputs smaller than kHostChunkMinBytes are not split.
@@ -86,9 +88,9 @@ struct gemm_ctx {
     // ready flag per epilogue warp (zero between launches)
     float *sk_ws = nullptr;
     uint32_t *sk_flags = nullptr;
-    // softmax epilogue: co-resident clusters of cs CTAs (one per 256 columns), per cs
-    // (0: that cluster size cannot be scheduled)
-    int row_clusters[kRowClusterMax + 1] = {};
+    // softmax kernel: co-resident clusters of cs = 1, 2, 4, 8 CTAs (0: that size cannot be
+    // scheduled; cs = 1 must be possible for the softmax epilogue to be offered at all)
+    int softmax_clusters[kSoftmaxClusterMax + 1] = {};
     // split-K: co-resident clusters of 2, 4 and 8 CTAs of the split-K instance, per size
     int split_clusters[9] = {};
     // gemm_run_host: device staging buffers, two copy streams and the events that order
@@ -167,12 +169,8 @@ int check_shape(const gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, int epilog
         return GEMM_ERR_ARG;
     if (M == 0 || N == 0)
         return GEMM_OK;
-    if (epilogue == GEMM_EPI_SOFTMAX) {
-        // a row takes a cluster of ceil(N / 256) CTAs
-        const int64_t cs = (N + kSoftmaxTileN - 1) / kSoftmaxTileN;
-        if (cs > kRowClusterMax || ctx->row_clusters[cs] == 0)
-            return GEMM_ERR_ARG;
-    }
+    if (epilogue == GEMM_EPI_SOFTMAX && ctx->softmax_clusters[1] == 0)
+        return GEMM_ERR_ARG;   // the device cannot run the softmax kernel
     if (N % 8 != 0 || K % 8 != 0)
         return GEMM_ERR_ALIGN;
     return GEMM_OK;
@@ -257,14 +255,16 @@ void launch_pdl_cluster(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, gb
 
 // The kernel instance gemm_run launches for a problem, with its grid and the schedule fields
 // of its parameters. make_plan decides; launch runs the plan; gemm_describe reports it.
-enum PlanKind : int { PLAN_PAIR, PLAN_TILES, PLAN_TILES8, PLAN_STREAMK, PLAN_SPLITK, PLAN_ROWCLUSTER };
+enum PlanKind : int {
+    PLAN_PAIR, PLAN_TILES, PLAN_TILES8, PLAN_STREAMK, PLAN_SPLITK, PLAN_ROWCLUSTER, PLAN_ROWCLUSTER2
+};
 
 struct Plan {
     PlanKind kind = PLAN_TILES;
     int grid = 0;      // CTAs launched
     int cluster = 1;   // CTAs per thread-block cluster (1: no cluster attribute)
     int m_blocks = 0, n_blocks = 0, num_tiles = 0, group_m = 1;
-    int split = 0, row_cluster = 0;
+    int split = 0, row_cluster = 0, smx_span = 0, smx_two_pass = 0;
     int64_t sk_units = 0;
 };
 
@@ -276,7 +276,8 @@ const char *plan_kernel_name(PlanKind k)
     case PLAN_TILES8: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,8>,SCHED_TILES>";
     case PLAN_STREAMK: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_STREAM_K>";
     case PLAN_SPLITK: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,8>,SCHED_SPLIT_K>";
-    case PLAN_ROWCLUSTER: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,8>,SCHED_ROW_CLUSTER>";
+    case PLAN_ROWCLUSTER: return "gemm_softmax_kernel<SoftmaxConfig<3>,false>";
+    case PLAN_ROWCLUSTER2: return "gemm_softmax_kernel<SoftmaxConfig<3>,true>";
     }
     return "unknown";
 }
@@ -288,18 +289,42 @@ Plan make_plan(const gemm_ctx *ctx, int M, int N, int K, int epilogue)
     Plan pl;
     const int num_kb = (K + Cfg::BK - 1) / Cfg::BK;
     if (epilogue == GEMM_EPI_SOFTMAX) {
-        // one cluster of n_blocks CTAs (a single CTA when N <= 256) per 128-row block
-        static_assert(Cfg8::BM == Cfg::BM && Cfg8::BN == Cfg::BN && Cfg8::BK == Cfg::BK &&
-                          Cfg8::B_BOX_N == Cfg::B_BOX_N,
+        static_assert(SoftCfg::BM == Cfg::BM && SoftCfg::BN == Cfg::BN && SoftCfg::BK == Cfg::BK &&
+                          SoftCfg::B_BOX_N == Cfg::B_BOX_N,
                       "same tensor-map boxes as the GEMM kernel");
         pl.kind = PLAN_ROWCLUSTER;
-        pl.m_blocks = (M + Cfg8::BM - 1) / Cfg8::BM;
-        pl.n_blocks = (N + Cfg8::BN - 1) / Cfg8::BN;
+        pl.m_blocks = (M + SoftCfg::BM - 1) / SoftCfg::BM;
+        pl.n_blocks = (N + SoftCfg::BN - 1) / SoftCfg::BN;
         pl.num_tiles = pl.m_blocks * pl.n_blocks;
         pl.group_m = 1;
-        pl.row_cluster = pl.n_blocks;
-        pl.cluster = pl.n_blocks;
-        pl.grid = std::min(pl.m_blocks, ctx->row_clusters[pl.n_blocks]) * pl.n_blocks;
+        int cs = 1, span = 1;
+        if (pl.n_blocks > 1) {
+            // Two passes over each CTA's span of column tiles. Cluster size: the one that
+            // minimises the tile epilogues of the busiest CTA, rounds x (2 x span + 1 for the
+            // statistics exchange when cs > 1), with the co-resident clusters of that size;
+            // ties go to the smaller cluster.
+            int64_t best = INT64_MAX;
+            for (int c = 1; c <= kSoftmaxClusterMax; c *= 2) {
+                const int conc = std::min(pl.m_blocks, ctx->softmax_clusters[c]);
+                if (conc <= 0)
+                    continue;
+                const int sp = (pl.n_blocks + c - 1) / c;
+                const int64_t rounds = (pl.m_blocks + conc - 1) / conc;
+                const int64_t cost = rounds * (2 * sp + (c > 1 ? 1 : 0));
+                if (cost < best) {
+                    best = cost;
+                    cs = c;
+                    span = sp;
+                }
+            }
+        }
+        pl.row_cluster = cs;
+        pl.smx_span = span;
+        pl.smx_two_pass = pl.n_blocks > 1 ? 1 : 0;
+        if (pl.smx_two_pass)
+            pl.kind = PLAN_ROWCLUSTER2;
+        pl.cluster = cs;
+        pl.grid = std::min(pl.m_blocks, ctx->softmax_clusters[cs]) * cs;
         return pl;
     }
     // 256 x 256 tiles on CTA pairs when there are enough of them to give every pair at
@@ -405,6 +430,8 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     p.group_m = pl.group_m;
     p.split = pl.split;
     p.row_cluster = pl.row_cluster;
+    p.smx_span = pl.smx_span;
+    p.smx_two_pass = pl.smx_two_pass;
     if (pl.kind == PLAN_STREAMK) {
         p.sk_units = pl.sk_units;
         p.sk_ws = ctx->sk_ws;
@@ -412,8 +439,13 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     }
     switch (pl.kind) {
     case PLAN_ROWCLUSTER:
-        launch_pdl_cluster(gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_ROW_CLUSTER>, pl.grid, pl.cluster,
-                           Cfg8::NUM_THREADS, Cfg8::SMEM_BYTES, stream, ta, tb, tc, p);
+    case PLAN_ROWCLUSTER2:
+        if (pl.smx_two_pass)
+            launch_pdl_cluster(gb300::gemm_softmax_kernel<SoftCfg, true>, pl.grid, pl.cluster, SoftCfg::NUM_THREADS,
+                               SoftCfg::SMEM_BYTES, stream, ta, tb, tc, p);
+        else
+            launch_pdl_cluster(gb300::gemm_softmax_kernel<SoftCfg, false>, pl.grid, pl.cluster, SoftCfg::NUM_THREADS,
+                               SoftCfg::SMEM_BYTES, stream, ta, tb, tc, p);
         break;
     case PLAN_PAIR:
         launch_pdl(gb300::gemm_tcgen05_pair_kernel<PairCfg>, pl.grid, PairCfg::NUM_THREADS, PairCfg::SMEM_BYTES,
@@ -538,18 +570,18 @@ int gemm_create(gemm_ctx **out, int device)
         }
         cudaGetLastError();
     }
-    // Softmax row clusters: how many clusters of each size fit at once (sizes above 8 need
-    // the non-portable cluster attribute; a size that cannot be scheduled stays 0 and the
-    // widths it would serve are refused).
+    // Softmax kernel: how many clusters of 1, 2, 4 and 8 CTAs fit at once (a size that
+    // cannot be scheduled stays 0 and is not used).
     {
-        auto *rk = gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_ROW_CLUSTER>;
-        if (cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg8::SMEM_BYTES) == cudaSuccess &&
-            cudaFuncSetAttribute(rk, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
-            for (int cs = 1; cs <= kRowClusterMax; ++cs) {
+        auto *sk = gb300::gemm_softmax_kernel<SoftCfg, true>;   // same resources as <SoftCfg, false>
+        if (cudaFuncSetAttribute(gb300::gemm_softmax_kernel<SoftCfg, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SoftCfg::SMEM_BYTES) == cudaSuccess &&
+            cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SoftCfg::SMEM_BYTES) == cudaSuccess) {
+            for (int cs = 1; cs <= kSoftmaxClusterMax; cs *= 2) {
                 cudaLaunchConfig_t lc = {};
                 lc.gridDim = dim3(static_cast<unsigned>(cs * (sms / cs)), 1, 1);
-                lc.blockDim = dim3(Cfg8::NUM_THREADS, 1, 1);
-                lc.dynamicSmemBytes = Cfg8::SMEM_BYTES;
+                lc.blockDim = dim3(SoftCfg::NUM_THREADS, 1, 1);
+                lc.dynamicSmemBytes = SoftCfg::SMEM_BYTES;
                 cudaLaunchAttribute a[1];
                 a[0].id = cudaLaunchAttributeClusterDimension;
                 a[0].val.clusterDim.x = static_cast<unsigned>(cs);
@@ -558,8 +590,8 @@ int gemm_create(gemm_ctx **out, int device)
                 lc.attrs = a;
                 lc.numAttrs = 1;
                 int n = 0;
-                if (cudaOccupancyMaxActiveClusters(&n, rk, &lc) == cudaSuccess)
-                    ctx->row_clusters[cs] = n;
+                if (cudaOccupancyMaxActiveClusters(&n, sk, &lc) == cudaSuccess)
+                    ctx->softmax_clusters[cs] = n;
             }
         }
         cudaGetLastError();

@@ -31,14 +31,6 @@
 //    flag; the owner waits for the flags, pulls each partial into its (by then idle) operand
 //    ring with one bulk copy per warp, adds it to the accumulator in Tensor Memory, runs the
 //    epilogue and lowers the flags again for the next launch.
-//  * row clusters (the softmax epilogue over rows wider than one tile, 256 < N <= 4096): a
-//    thread-block cluster of ceil(N / 256) CTAs owns a 128-row block, CTA r computing column
-//    tile r. Each epilogue thread reduces its row over its CTA's columns (running maximum and
-//    sum of exponentials), the CTAs exchange these per-row statistics through distributed
-//    shared memory (mbarrier arrivals on every CTA of the cluster, then ld.shared::cluster),
-//    and each CTA normalises its own tile from Tensor Memory: the logits never leave the
-//    chip and C is written once.
-//
 // Every mbarrier wait is bounded in time. When a wait runs out the kernel records which
 // one in a device error word, tells the other roles to stop, waits (bounded) for its own
 // copies and MMAs in flight, frees its Tensor Memory and returns.
@@ -68,7 +60,6 @@ enum : uint32_t {
 enum : int {
     SCHED_TILES = 0,         // whole tiles, grouped raster, persistent
     SCHED_STREAM_K = 1,      // equal ranges of (tile, k-block) units
-    SCHED_ROW_CLUSTER = 2,   // one cluster per 128-row block, CTA r = column tile r
     SCHED_SPLIT_K = 3,       // one cluster per tile, CTA r = the r-th of `split` equal k ranges
 };
 
@@ -95,7 +86,9 @@ struct GemmParams {
     int64_t sk_units = 0;
     float *sk_ws = nullptr;          // [gridDim.x][epilogue warp][chunk][8][32 lanes][4] FP32 partials
     uint32_t *sk_flags = nullptr;    // [gridDim.x][epilogue warps]: 1 = that part is written
-    int row_cluster = 0;             // row clusters: CTAs per cluster (= n_blocks)
+    int row_cluster = 0;             // softmax kernel: CTAs per cluster (1, 2, 4 or 8)
+    int smx_span = 0;                // softmax kernel: column tiles per CTA of a cluster
+    int smx_two_pass = 0;            // softmax kernel: 1 = statistics pass, then output pass
     int split = 0;                   // split-K: CTAs per cluster, each with 1/split of the k-blocks
     int64_t ldc = 0;                 // row stride of C in elements (split-K writes C directly)
 };
@@ -119,8 +112,8 @@ struct KernelConfig {
     static constexpr int EPI_COL_GROUPS = NUM_EPI_WARPS / 4;   // warps sharing a TMEM quarter
     static constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
     // full[s], empty[s], acc_full[b], acc_empty[b], drain, one stream-K partial barrier per
-    // epilogue warp, row-cluster stats_ready[2] and stats_read[2]
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + NUM_EPI_WARPS + 4;
+    // epilogue warp
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + NUM_EPI_WARPS;
     // stream-K: one epilogue warp's share of a partial accumulator (32 rows x its columns,
     // FP32), as stored in the workspace and as pulled into the operand ring
     static constexpr int PART_WARP_BYTES = (BN / EPI_COL_GROUPS) * 32 * 4;
@@ -129,12 +122,7 @@ struct KernelConfig {
     static constexpr int BIAS_OFFSET = STAGES * STAGE_BYTES + ((NUM_BARS * 8 + 16 + 15) / 16) * 16;
     // then, 1024-aligned, two 32 x 32 FP16 output staging boxes per epilogue warp
     static constexpr int STORE_OFFSET = ((BIAS_OFFSET + NUM_EPI_WARPS * BN * 2 + 1023) / 1024) * 1024;
-    // then the softmax row statistics: the cluster exchange's two buffers of (max, sum) per
-    // row, and (two column groups) the groups' two buffers of (max, sum) per row and group
-    static constexpr int STATS_OFFSET = STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES;
-    static constexpr int PAIR_OFFSET = STATS_OFFSET + 2 * BM * 8;
-    static constexpr int SMEM_BYTES =
-        1024 /* alignment slack */ + PAIR_OFFSET + (EPI_COL_GROUPS == 2 ? 2 * BM * 2 * 8 : 0);
+    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES;
 
     static_assert(BM == 128, "one CTA, M = 128: TMEM lane i holds tile row i");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
@@ -190,8 +178,6 @@ __device__ __forceinline__ int64_t sk_begin(const GemmParams &p, int g)
 // The work of this CTA as segments: k-blocks [k0, k1) of output tile t = (mb, nb).
 //  SCHED_TILES: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ... in the grouped raster.
 //  SCHED_STREAM_K: the pieces of the tiles that the CTA's unit range covers, in order.
-//  SCHED_ROW_CLUSTER: row blocks clusterid, clusterid + clusters, ...; column tile = the
-//  CTA's rank in its cluster.
 //  SCHED_SPLIT_K: tile clusterid; k-blocks [r * num_kb / split, (r + 1) * num_kb / split) for
 //  the CTA of rank r (never empty when num_kb >= split).
 template <int SCHED>
@@ -203,10 +189,6 @@ struct WorkIter {
         if constexpr (SCHED == SCHED_STREAM_K) {
             u = sk_begin(p, static_cast<int>(blockIdx.x));
             end = sk_begin(p, static_cast<int>(blockIdx.x) + 1);
-        } else if constexpr (SCHED == SCHED_ROW_CLUSTER) {
-            t = static_cast<int>(cluster_id_x());
-            step = static_cast<int>(cluster_count_x());
-            rank = static_cast<int>(cluster_ctarank());
         } else if constexpr (SCHED == SCHED_SPLIT_K) {
             t = static_cast<int>(cluster_id_x());
             rank = static_cast<int>(cluster_ctarank());
@@ -234,16 +216,6 @@ struct WorkIter {
             tile_coords(p, tile, mb, nb);
             k0 = static_cast<int>(static_cast<int64_t>(rank) * p.num_kb / p.split);
             k1 = static_cast<int>(static_cast<int64_t>(rank + 1) * p.num_kb / p.split);
-            return true;
-        } else if constexpr (SCHED == SCHED_ROW_CLUSTER) {
-            if (t >= p.m_blocks)
-                return false;
-            mb = t;
-            nb = rank;
-            tile = mb * p.n_blocks + nb;
-            k0 = 0;
-            k1 = p.num_kb;
-            t += step;
             return true;
         } else {
             if (t >= p.num_tiles)
@@ -417,22 +389,6 @@ __device__ __forceinline__ void epilogue_math_stage(const GemmParams &p, const u
     }
 }
 
-// Row softmax epilogue: what one epilogue warp needs to merge its rows' statistics with those
-// of the other warps covering the same rows (the other column group of its CTA, and the CTAs
-// of a row cluster) for one tile.
-struct RowExchange {
-    uint32_t stats;    // cluster exchange: [2 buffers][128 rows] x (max, sum) of this CTA
-    uint32_t pair;     // column groups: [2 buffers][128 rows][2 groups] x (max, sum)
-    uint32_t ready0;   // stats_ready[2]: one warp per lane quarter of every CTA has published
-    uint32_t read0;    // stats_read[2]: every epilogue warp of every CTA has read this buffer
-    int cs;            // CTAs in the cluster (1: no cluster exchange)
-    int quarter;       // this warp's TMEM lane quarter
-    int group;         // this warp's column group
-    uint32_t buf;      // buffer of this tile (tile count % 2)
-    uint32_t use;      // earlier uses of that buffer (tile count / 2)
-    const WaitCtl *wc;
-};
-
 // Bounded wait on a local barrier whose phase is completed by arrivals from the cluster.
 __device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity, const WaitCtl &w, uint32_t code)
 {
@@ -463,245 +419,6 @@ __device__ __forceinline__ void merge_stats(float &M, float &S, float m, float s
     } else {
         S += s * ex2_approx(m - M);
     }
-}
-
-// Row statistics exchange, step 1: turn this thread's statistics of its row piece (m:
-// maximum in base-2 units, s: sum of 2^(x - m)) into those of the CTA's part of the row and,
-// in a cluster, publish them. With two column groups the pair of warps of a lane quarter
-// merge through shared memory behind a 64-thread named barrier. In a cluster the group-0
-// warp writes the CTA's row statistics and arrives on every CTA's stats_ready barrier (lane r
-// on CTA r: one instruction for all). All 32 lanes call it; false if a wait ran out.
-template <int GROUPS>
-__device__ __forceinline__ bool row_publish(const RowExchange &x, float &m, float &s, int row, int lane)
-{
-    static_assert(GROUPS == 1 || GROUPS == 2, "one or two column groups");
-    if constexpr (GROUPS == 2) {
-        const uint32_t slot = x.pair + ((x.buf * 128u + static_cast<uint32_t>(row)) * 2u) * 8u;
-        st_shared_f2(slot + static_cast<uint32_t>(x.group) * 8u, m, s);
-        named_barrier_sync(1u + static_cast<uint32_t>(x.quarter), 64u);
-        const float2 o = ld_shared_f2(slot + static_cast<uint32_t>(x.group ^ 1) * 8u);
-        merge_stats(m, s, o.x, o.y);
-    }
-    if (x.cs == 1 || x.group != 0)
-        return true;
-    int ok = 1;
-    if (x.use > 0 && lane == 0)   // everyone has read what this buffer held last time
-        ok = wait_cluster_bounded(x.read0 + 8u * x.buf, (x.use - 1u) & 1u, *x.wc, ERR_ROW_EXCHANGE) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, ok, 0))
-        return false;
-    st_shared_f2(x.stats + (x.buf * 128u + static_cast<uint32_t>(row)) * 8u, m, s);
-    __syncwarp();
-    if (lane < x.cs)   // release: the statistics above
-        mbar_arrive_cluster(mapa_shared(x.ready0 + 8u * x.buf, static_cast<uint32_t>(lane)));
-    return true;
-}
-
-// Step 2 (clusters only): wait until every CTA has published, read every CTA's entry for
-// this row through distributed shared memory (all reads issued before the merge), merge
-// them into the whole row's (m, s) and arrive on every CTA's stats_read barrier. All 32
-// lanes call it; false if a wait ran out.
-__device__ __forceinline__ bool row_collect(const RowExchange &x, float &m, float &s, int row, int lane)
-{
-    if (x.cs == 1)
-        return true;
-    int ok = 1;
-    if (lane == 0)
-        ok = wait_cluster_bounded(x.ready0 + 8u * x.buf, x.use & 1u, *x.wc, ERR_ROW_EXCHANGE) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, ok, 0))
-        return false;
-    const uint32_t slot = x.stats + (x.buf * 128u + static_cast<uint32_t>(row)) * 8u;
-    float M = -INFINITY, S = 0.0f;
-#pragma unroll
-    for (int r0 = 0; r0 < 16; r0 += 8) {
-        if (r0 >= x.cs)
-            break;
-        float2 v[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-            if (r0 + r < x.cs)
-                v[r] = ld_shared_cluster_f2(mapa_shared(slot, static_cast<uint32_t>(r0 + r)));
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-            if (r0 + r < x.cs)
-                merge_stats(M, S, v[r].x, v[r].y);
-    }
-    __syncwarp();
-    if (lane < x.cs)   // release: the reads above
-        mbar_arrive_cluster(mapa_shared(x.read0 + 8u * x.buf, static_cast<uint32_t>(lane)));
-    m = M;
-    s = S;
-    return true;
-}
-
-// Row-softmax epilogue ("Designing High-Performance GPU Kernels with TileLang", spaxe.top:
-// softmax applied to each row of the GEMM result in the epilogue, no intermediate written to
-// global memory). Each thread owns one row (its TMEM lane) and this warp's CHUNKS chunks of
-// 32 columns of it (chunks [0, valid) lie inside C; `active`: the warp's rows start inside C).
-//
-// Pass 1, per chunk: logits (+ bias) in base-2 units, the chunk maximum mc[c], p = 2^(x - mc)
-// written back over the accumulator in TMEM, and the chunk's sum of p, merged into (m, s).
-// One exponential per element; columns at or past N contribute nothing.
-template <int CHUNKS>
-__device__ __forceinline__ void softmax_pass1(const GemmParams &p, uint32_t taddr, int n_first, int valid, bool active,
-                                              const uint4 *sbias, float (&mc)[CHUNKS], float &m, float &s)
-{
-    constexpr float kL2e = 1.4426950408889634f;
-    const bool has_acc = p.num_kb > 0;
-    m = -INFINITY;
-    s = 0.0f;
-#pragma unroll
-    for (int c = 0; c < CHUNKS; ++c) {
-        mc[c] = -INFINITY;
-        if (!active || c >= valid)
-            continue;
-        uint32_t r[32];
-        if (has_acc) {
-            tmem_ld_32x32b_x32(taddr + 32u * c, r);
-            tmem_ld_wait_regs(r);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                r[j] = 0u;
-        }
-        float v[32];
-        if (sbias != nullptr) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 bv = sbias[4 * c + i];
-                const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(bh[e]);
-                    const uint64_t t = f32x2_mul(f32x2_add(f32x2_pack(__uint_as_float(r[8 * i + 2 * e]),
-                                                                      __uint_as_float(r[8 * i + 2 * e + 1])),
-                                                           f32x2_pack(f.x, f.y)),
-                                                 f32x2_pack(kL2e, kL2e));
-                    f32x2_unpack(t, v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                const uint64_t t = f32x2_mul(f32x2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                                             f32x2_pack(kL2e, kL2e));
-                f32x2_unpack(t, v[j], v[j + 1]);
-            }
-        }
-        const int n0 = n_first + 32 * c;
-        if (n0 + 32 > p.N) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (n0 + j >= p.N)
-                    v[j] = -INFINITY;   // not a column of C: contributes 2^-inf = 0
-        }
-        // chunk maximum in four independent three-input chains
-        float q0 = fmax3(v[0], v[1], v[2]), q1 = fmax3(v[3], v[4], v[5]);
-        float q2 = fmax3(v[6], v[7], v[8]), q3 = fmax3(v[9], v[10], v[11]);
-#pragma unroll
-        for (int j = 12; j < 28; j += 8) {
-            q0 = fmax3(q0, v[j], v[j + 1]);
-            q1 = fmax3(q1, v[j + 2], v[j + 3]);
-            q2 = fmax3(q2, v[j + 4], v[j + 5]);
-            q3 = fmax3(q3, v[j + 6], v[j + 7]);
-        }
-        q0 = fmax3(q0, v[28], v[29]);
-        q1 = fmax3(q1, v[30], v[31]);
-        const float cm = fmax3(fmaxf(q0, q1), q2, q3);
-        // 2^(v - cm), summed in two packed partial sums
-        const uint64_t neg_cm = f32x2_pack(-cm, -cm);
-        uint64_t sa = f32x2_pack(0.0f, 0.0f), sb = sa;
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-            float d0, d1;
-            f32x2_unpack(f32x2_add(f32x2_pack(v[j], v[j + 1]), neg_cm), d0, d1);
-            const float e0 = ex2_approx(d0), e1 = ex2_approx(d1);
-            if ((j & 2) == 0)
-                sa = f32x2_add(sa, f32x2_pack(e0, e1));
-            else
-                sb = f32x2_add(sb, f32x2_pack(e0, e1));
-            r[j] = __float_as_uint(e0);
-            r[j + 1] = __float_as_uint(e1);
-        }
-        float s0, s1;
-        f32x2_unpack(f32x2_add(sa, sb), s0, s1);
-        const float cs = s0 + s1;
-        tmem_st_32x32b_x32(taddr + 32u * c, r);
-        mc[c] = cm;
-        merge_stats(m, s, cm, cs);
-    }
-    if (active)
-        tmem_st_wait();
-}
-
-// Pass 2, with the whole row's (m, s): every p of chunk c times 2^(mc[c] - m) / s, to FP16,
-// staged in the warp's 32 x 32 boxes and written by TMA.
-template <int CHUNKS>
-__device__ __forceinline__ void softmax_pass2(uint32_t taddr, int n_first, int row0, int valid,
-                                              const float (&mc)[CHUNKS], float m, float s,
-                                              const CUtensorMap *tmap_c, uint32_t stage, uint32_t &box_sel, int lane)
-{
-    const float inv = 1.0f / s;
-#pragma unroll
-    for (int c = 0; c < CHUNKS; ++c) {
-        if (c >= valid)
-            break;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + 32u * c, r);
-        const float scale = ex2_approx(mc[c] - m) * inv;
-        tmem_ld_wait_regs(r);
-        const uint32_t box = stage + box_sel * EPI_STORE_BOX_BYTES;
-        if (lane == 0)
-            bulk_wait_group_read<1>();
-        __syncwarp();
-        const uint32_t row_base = box + static_cast<uint32_t>(lane) * 64u;
-        const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint64_t q = f32x2_mul(f32x2_pack(__uint_as_float(r[8 * i + 2 * e]),
-                                                        __uint_as_float(r[8 * i + 2 * e + 1])),
-                                             f32x2_pack(scale, scale));
-                float a, b;
-                f32x2_unpack(q, a, b);
-                __half2 h = __floats2half2_rn(a, b);
-                w[e] = *reinterpret_cast<uint32_t *>(&h);
-            }
-            st_shared_v4(row_base + ((static_cast<uint32_t>(i) ^ sw) << 4), make_uint4(w[0], w[1], w[2], w[3]));
-        }
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_2d(tmap_c, box, n_first + 32 * c, row0, l2_policy_evict_first());
-            bulk_commit_group();
-        }
-        box_sel ^= 1u;
-    }
-}
-
-// The whole softmax epilogue of one tile: pass 1, the row statistics exchange (with `xch`:
-// several warps or CTAs cover the row), pass 2. Without `xch` the warp must cover every
-// column of C (N <= CHUNKS * 32).
-template <int CHUNKS, int GROUPS>
-__device__ __forceinline__ void epilogue_softmax_tile(const GemmParams &p, uint32_t taddr, int n_first, int row0,
-                                                      const uint4 *sbias, const CUtensorMap *tmap_c,
-                                                      uint32_t stage, uint32_t &box_sel, int lane,
-                                                      const RowExchange *xch)
-{
-    const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
-    const bool active = valid > 0 && row0 < p.M;
-    if (!active && xch == nullptr)
-        return;   // (a warp of an exchange still publishes and reads statistics)
-    float mc[CHUNKS], m, s;
-    softmax_pass1<CHUNKS>(p, taddr, n_first, valid, active, sbias, mc, m, s);
-    if (xch != nullptr) {
-        const int row = static_cast<int>(row0 % 128) + lane;
-        if (!row_publish<GROUPS>(*xch, m, s, row, lane) || !row_collect(*xch, m, s, row, lane))
-            return;
-    }
-    if (active)
-        softmax_pass2<CHUNKS>(taddr, n_first, row0, valid, mc, m, s, tmap_c, stage, box_sel, lane);
 }
 
 // Stream-K: a CTA holding a later part of a tile writes its warp's share of the FP32
@@ -807,15 +524,11 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *flag, const WaitCtl &w
 // each finished 32 x 32 box goes out with one TMA store from the warp's two alternating
 // staging boxes (`stage`, toggled through `box_sel`), which clips rows >= M and
 // columns >= N. Called by all 32 lanes together (tcgen05.ld is warp-collective).
-template <int CHUNKS, int GROUPS = 1>
+template <int CHUNKS>
 __device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t taddr, int n_first, int row0,
                                               const uint4 *sbias, const CUtensorMap *tmap_c, uint32_t stage,
-                                              uint32_t &box_sel, int lane, const RowExchange *xch = nullptr)
+                                              uint32_t &box_sel, int lane)
 {
-    if (p.epilogue == EPI_SOFTMAX) {
-        epilogue_softmax_tile<CHUNKS, GROUPS>(p, taddr, n_first, row0, sbias, tmap_c, stage, box_sel, lane, xch);
-        return;
-    }
     const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
     if (valid <= 0 || row0 >= p.M)
         return;   // nothing of this warp's part of the tile is inside C
@@ -985,8 +698,8 @@ __device__ __forceinline__ void splitk_reduce(const GemmParams &p, uint32_t stag
 }
 
 // SCHED: SCHED_TILES (whole tiles per CTA), SCHED_STREAM_K (p.sk_units > 0, workspace and
-// flags set) or SCHED_ROW_CLUSTER (launched in clusters of p.row_cluster = n_blocks CTAs,
-// softmax epilogue only).
+// flags set) or SCHED_SPLIT_K (launched in clusters of p.split CTAs). Epilogues NONE, GELU
+// and RELU (the softmax epilogue has a kernel of its own).
 template <class Cfg, int SCHED = SCHED_TILES>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -1008,7 +721,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const uint32_t full0 = bar0, empty0 = bar0 + 8u * STAGES;
     const uint32_t accf0 = bar0 + 16u * STAGES, acce0 = accf0 + 8u * Cfg::ACC_BUFS;
     const uint32_t drain = acce0 + 8u * Cfg::ACC_BUFS, part0 = drain + 8u;
-    const uint32_t stats_ready0 = part0 + 8u * Cfg::NUM_EPI_WARPS, stats_read0 = stats_ready0 + 16u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     uint4 *bias_stage = reinterpret_cast<uint4 *>(sp + Cfg::BIAS_OFFSET);
@@ -1029,14 +741,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         mbar_init(drain, 1);
         for (int w = 0; w < Cfg::NUM_EPI_WARPS; ++w)
             mbar_init(part0 + 8u * w, 1);
-        // row clusters: one warp per lane quarter of every CTA publishes, every epilogue warp
-        // of every CTA reads, once per phase
-        const uint32_t pub = SCHED == SCHED_ROW_CLUSTER ? static_cast<uint32_t>(p.row_cluster * 4) : 1u;
-        const uint32_t rd = SCHED == SCHED_ROW_CLUSTER ? static_cast<uint32_t>(p.row_cluster * Cfg::NUM_EPI_WARPS) : 1u;
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(stats_ready0 + 8u * b, pub);
-            mbar_init(stats_read0 + 8u * b, rd);
-        }
         *abort_flag = 0;
         fence_mbar_init();
         if (p.num_kb > 0) {
@@ -1044,10 +748,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             tma_prefetch_desc(&tmap_b);
         }
         tma_prefetch_desc(&tmap_c);
-    }
-    if constexpr (SCHED == SCHED_ROW_CLUSTER) {
-        __syncwarp();
-        cluster_sync();   // every CTA's barriers exist before any remote arrival
     }
     if (warp == 1) {
         tmem_alloc<1>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -1188,84 +888,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                                              quarter * 32 + lane, c_begin);
                 }
             }
-        } else if constexpr (SCHED == SCHED_ROW_CLUSTER) {
-            // Softmax over a row cluster, pipelined by one tile: pass 1 and the publication of
-            // tile i's row statistics come before the collection and pass 2 of tile i - 1, so
-            // that waiting for the other CTAs overlaps work (both TMEM accumulators hold a tile).
-            // A single CTA per row (N <= 256) has nothing to wait for and finishes each tile at
-            // once, which frees its accumulator for the next MMAs sooner.
-            struct Pending {
-                RowExchange x;
-                uint32_t taddr;
-                int n_first, row0, valid, acc;
-                bool active;
-                float m, s, mc[CHUNKS];
-            };
-            const int row = quarter * 32 + lane;
-            const int group = (warp - 2) >> 2;
-            Pending pend;
-            bool have = false;
-            uint32_t tiles = 0;
-            WorkIter<SCHED> work(p);
-            int t, mb, nb, k0, k1;
-            for (;;) {
-                const bool got = work.next(p, t, mb, nb, k0, k1);
-                Pending cur;
-                if (got) {
-                    const uint4 bv = bias_fetch(p, nb * BN, lane);
-                    int ok = 1;
-                    if (lane == 0)
-                        ok = wait_bounded(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
-                    if (!__shfl_sync(0xffffffffu, ok, 0))
-                        break;
-                    tc_fence_after_sync();
-                    if (p.bias != nullptr) {
-                        my_bias[lane] = bv;
-                        __syncwarp();
-                    }
-                    cur.taddr = tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c_begin * 32);
-                    cur.n_first = nb * BN + c_begin * 32;
-                    cur.row0 = mb * BM + quarter * 32;
-                    cur.valid = min(CHUNKS, (p.N - cur.n_first + 31) / 32);
-                    cur.active = cur.valid > 0 && cur.row0 < p.M;
-                    cur.acc = acc;
-                    softmax_pass1<CHUNKS>(p, cur.taddr, cur.n_first, cur.valid, cur.active,
-                                          p.bias != nullptr ? my_bias + c_begin * 4 : nullptr, cur.mc, cur.m, cur.s);
-                    cur.x = RowExchange{base + Cfg::STATS_OFFSET, base + Cfg::PAIR_OFFSET, stats_ready0, stats_read0,
-                                        p.row_cluster, quarter, group, tiles & 1u, tiles >> 1, &wc};
-                    if (!row_publish<Cfg::EPI_COL_GROUPS>(cur.x, cur.m, cur.s, row, lane))
-                        break;
-                    ++tiles;
-                    if (++acc == Cfg::ACC_BUFS) {
-                        acc = 0;
-                        acc_phase ^= 1u;
-                    }
-                }
-                auto finish = [&](Pending &f) -> bool {
-                    if (!row_collect(f.x, f.m, f.s, row, lane))
-                        return false;
-                    if (f.active)
-                        softmax_pass2<CHUNKS>(f.taddr, f.n_first, f.row0, f.valid, f.mc, f.m, f.s, &tmap_c, my_stage,
-                                              box_sel, lane);
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(acce0 + 8u * f.acc);   // this warp's rows of that accumulator are read
-                    return true;
-                };
-                if (have && !finish(pend))
-                    break;
-                if (!got)
-                    break;
-                if (p.row_cluster == 1) {
-                    if (!finish(cur))
-                        break;
-                    have = false;
-                } else {
-                    pend = cur;
-                    have = true;
-                }
-            }
         } else {
             WorkIter<SCHED> work(p);
             int t, mb, nb, k0, k1;
@@ -1361,8 +983,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (SCHED == SCHED_ROW_CLUSTER)
-        cluster_sync();   // no CTA leaves while another may still read its statistics
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);

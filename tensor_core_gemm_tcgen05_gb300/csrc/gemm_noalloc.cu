@@ -18,6 +18,7 @@
 
 #include "gemm.h"
 #include "gemm_kernel.cuh"
+#include "softmax_gemm_kernel.cuh"
 
 // The scratch of gemm_run_noalloc, GEMM_NOALLOC_SCRATCH_BYTES (256) bytes on every device.
 // Word 0 is the kernel's error word (which in-kernel wait ran out, 0 if none). In host code
@@ -30,6 +31,8 @@ namespace {
 // Same tile configuration as gemm_run's kernel, as a type of its own, so that this file's
 // kernel instance (and its shared-memory attribute) is separate from the one in gemm_api.cu.
 struct NoAllocCfg : gb300::KernelConfig<128, 256, 4> {};
+// The softmax epilogue's kernel (one CTA per 128-row block, N <= 256), likewise its own type.
+struct NoAllocSoftCfg : gb300::SoftmaxConfig<3> {};
 constexpr int kGroupM = 16;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kMaxDevices = 64;
@@ -55,13 +58,16 @@ void setup_device(DeviceSetup &s, int device)
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
-    if (major != 10 || minor != 3 || sms <= 0 || smem_optin < NoAllocCfg::SMEM_BYTES) {
+    if (major != 10 || minor != 3 || sms <= 0 || smem_optin < NoAllocCfg::SMEM_BYTES ||
+        smem_optin < NoAllocSoftCfg::SMEM_BYTES) {
         cudaGetLastError();
         s.status = GEMM_ERR_DEVICE;
         return;
     }
     if (cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<NoAllocCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             NoAllocCfg::SMEM_BYTES) != cudaSuccess) {
+                             NoAllocCfg::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(gb300::gemm_softmax_kernel<NoAllocSoftCfg, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, NoAllocSoftCfg::SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         s.status = GEMM_ERR_DEVICE;
         return;
@@ -194,7 +200,28 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
     p.timeout_ns = kTimeoutNs;
     p.debug = 0;
     const int grid = p.num_tiles < s.num_sms ? p.num_tiles : s.num_sms;
-    gb300::gemm_tcgen05_kernel<NoAllocCfg><<<grid, NoAllocCfg::NUM_THREADS, NoAllocCfg::SMEM_BYTES, st>>>(ta, tb, tc, p);
+    if (epilogue == GEMM_EPI_SOFTMAX) {
+        // the row fits one tile: one CTA per 128-row block (a cluster of one), a single pass
+        p.row_cluster = 1;
+        p.smx_span = 1;
+        p.smx_two_pass = 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+        cfg.blockDim = dim3(NoAllocSoftCfg::NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = NoAllocSoftCfg::SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, gb300::gemm_softmax_kernel<NoAllocSoftCfg, false>, ta, tb, tc, p);
+    } else {
+        gb300::gemm_tcgen05_kernel<NoAllocCfg><<<grid, NoAllocCfg::NUM_THREADS, NoAllocCfg::SMEM_BYTES, st>>>(ta, tb, tc,
+                                                                                                          p);
+    }
     if (cudaGetLastError() != cudaSuccess)
         return GEMM_ERR_LAUNCH;
     return GEMM_OK;

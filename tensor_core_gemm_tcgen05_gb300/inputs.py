@@ -84,10 +84,18 @@ WORKLOADS: dict[str, Workload] = {
         # keys N(0,1/K) so the logits are about N(0,1).
         Workload("scores_262144x256x128_softmax", 262144, 256, 128, "softmax", False,
                  a_dist="normal", b_dist="normal_inv_k", sample_rows=512, include_last=8),
-        # The same over rows wider than one tile (a cluster of 4 CTAs per 128-row block):
-        # 32768 queries against 1024 keys.
+        # The same over rows wider than one tile: 32768 queries against 512 to 2048 keys,
+        # 16384 against 4096 and 8192 against 16384.
+        Workload("scores_32768x512x128_softmax", 32768, 512, 128, "softmax", False,
+                 a_dist="normal", b_dist="normal_inv_k", sample_rows=256, include_last=8),
         Workload("scores_32768x1024x128_softmax", 32768, 1024, 128, "softmax", False,
                  a_dist="normal", b_dist="normal_inv_k", sample_rows=256, include_last=8),
+        Workload("scores_32768x2048x128_softmax", 32768, 2048, 128, "softmax", False,
+                 a_dist="normal", b_dist="normal_inv_k", sample_rows=256, include_last=8),
+        Workload("scores_16384x4096x128_softmax", 16384, 4096, 128, "softmax", False,
+                 a_dist="normal", b_dist="normal_inv_k", sample_rows=128, include_last=8),
+        Workload("scores_8192x16384x128_softmax", 8192, 16384, 128, "softmax", False,
+                 a_dist="normal", b_dist="normal_inv_k", sample_rows=64, include_last=4),
         # Few output tiles, long K: 32 tiles of 128 x 256 for ~150 SMs, the stream-K case.
         Workload("gemm_1024x1024x8192_bias_gelu", 1024, 1024, 8192, "gelu", True,
                  a_dist="normal", b_dist="normal_inv_k", bias_range=0.1, sample_rows=128, include_last=2),

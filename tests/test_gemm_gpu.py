@@ -208,16 +208,19 @@ def test_softmax_epilogue(kctx, shape, with_bias):
 
 
 WIDE_SOFTMAX = [(300, 264, 128), (129, 1000, 64), (257, 2048, 256), (200, 4096, 128), (4104, 512, 128),
-                (64, 3000, 320), (7, 776, 8)]
+                (64, 3000, 320), (7, 776, 8), (64, 4096, 128), (20000, 512, 64), (4104, 4104, 64),
+                (130, 8192, 64), (40, 16384, 128), (1000, 5000, 64)]
 
 
 @pytest.mark.parametrize("shape", WIDE_SOFTMAX, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("with_bias", [False, True])
 def test_softmax_epilogue_wide_rows(ctx, shape, with_bias):
-    """Rows wider than one tile: a cluster of ceil(N/256) CTAs (2 to 16, ragged last tile)
-    per 128-row block exchanges row statistics through distributed shared memory. Same bar
-    as the one-tile softmax: within one FP16 ulp of the oracle, rows sum to 1. 4104 rows =
-    33 row blocks, so clusters loop and reuse both statistics buffers many times."""
+    """Rows wider than one tile, any width: each CTA sweeps its span of column tiles twice
+    (row statistics, then outputs from recomputed logits), and a cluster of 1, 2, 4 or 8 CTAs
+    per 128-row block merges the statistics through distributed shared memory. Same bar as
+    the one-tile softmax: within one FP16 ulp of the oracle, rows sum to 1. Ragged last
+    tiles, ragged spans (CTAs without tiles), 4104 and 20000 rows (clusters loop over row
+    blocks and reuse both statistics buffers many times)."""
     M, N, K = shape
     A = inputs.random_fp16((M, K), 6300 + M, "normal")
     B = inputs.random_fp16((K, N), 6400 + N, "normal_inv_k", k=K)
@@ -253,14 +256,20 @@ def test_wide_softmax_timeout_then_recovery(ctx):
     test_softmax_epilogue_wide_rows(ctx, (300, 1000, 64), True)
 
 
+def test_softmax_cluster_sizes_are_covered(ctx):
+    """The wide-row shapes above reach every cluster size the softmax schedule uses (the
+    choice minimises the busiest CTA's tile epilogues; see gemm_describe)."""
+    seen = {}
+    for M, N, K in WIDE_SOFTMAX:
+        d = g.gemm_describe(ctx, M, N, K, g.EPI_SOFTMAX)
+        assert d.startswith("gemm_softmax_kernel<SoftmaxConfig<3>,true>"), d
+        seen[int(d.split("cluster=")[1].split()[0])] = (M, N, K)
+    assert {1, 2, 4, 8} <= set(seen), seen
+    assert g.gemm_describe(ctx, 300, 256, 128, g.EPI_SOFTMAX).startswith("gemm_softmax_kernel<SoftmaxConfig<3>,false>")
+
+
 def test_softmax_epilogue_limits(ctx):
     dev = torch.device("cuda:0")
-    A = torch.zeros(16, 64, dtype=torch.float16, device=dev)
-    B = torch.zeros(64, 4104, dtype=torch.float16, device=dev)
-    C = torch.zeros(16, 4104, dtype=torch.float16, device=dev)
-    with pytest.raises(g.GemmError) as e:      # 17 tiles per row: more than a cluster holds
-        g.gemm(ctx, A, B, None, g.EPI_SOFTMAX, out=C)
-    assert e.value.status == g.GEMM_ERR_ARG
     # K = 0 over a wide row: softmax of the bias
     bias_w = inputs.random_fp16((1536,), 98).to(dev)
     Cw = torch.empty(5, 1536, dtype=torch.float16, device=dev)
@@ -356,8 +365,8 @@ def test_describe_names_the_dispatched_kernel(ctx):
     d = g.gemm_describe
     assert d(ctx, 8200, 16384, 4096, g.EPI_GELU).startswith("gemm_tcgen05_pair_kernel<")
     assert "SCHED_SPLIT_K" in d(ctx, 1024, 1024, 8192, g.EPI_GELU)
-    wide = d(ctx, 32768, 1024, 128, g.EPI_SOFTMAX)
-    assert "SCHED_ROW_CLUSTER" in wide and "cluster=4" in wide
+    assert d(ctx, 262144, 256, 128, g.EPI_SOFTMAX).startswith("gemm_softmax_kernel<SoftmaxConfig<3>,false>")
+    assert d(ctx, 32768, 1024, 128, g.EPI_SOFTMAX).startswith("gemm_softmax_kernel<SoftmaxConfig<3>,true>")
     assert d(ctx, 0, 8, 8, g.EPI_NONE).startswith("none")
     with pytest.raises(g.GemmError) as e:
         d(ctx, 8, 60, 8, g.EPI_NONE)
