@@ -407,11 +407,13 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
                        CU_TENSOR_MAP_SWIZZLE_128B, static_cast<uint64_t>(ldb)))
             return GEMM_ERR_LAUNCH;
     }
-    // C is written by TMA in 32 x 32 boxes staged with the 64-byte swizzle
-    if (!encode_2d(ctx, &tc, C, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 32, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B, static_cast<uint64_t>(ldc)))
-        return GEMM_ERR_LAUNCH;
     const Plan pl = make_plan(ctx, M, N, K, epilogue);
+    // C is written by TMA in 32 x 32 boxes staged with the 64-byte swizzle; the softmax
+    // kernel writes 32-row x 64-column boxes staged with the 128-byte swizzle
+    const bool smx = pl.kind == PLAN_ROWCLUSTER || pl.kind == PLAN_ROWCLUSTER2;
+    if (!encode_2d(ctx, &tc, C, static_cast<uint64_t>(N), static_cast<uint64_t>(M), smx ? 64 : 32, 32,
+                   smx ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, static_cast<uint64_t>(ldc)))
+        return GEMM_ERR_LAUNCH;
     gb300::GemmParams p;
     p.M = M;
     p.N = N;

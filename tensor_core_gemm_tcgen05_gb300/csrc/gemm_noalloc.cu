@@ -174,8 +174,11 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
                        NoAllocCfg::BK))
             return GEMM_ERR_LAUNCH;
     }
-    if (!encode_2d(s.encode, &tc, C, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 32, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B))
+    // the GEMM kernel stores 32 x 32 boxes (64-byte swizzle), the softmax kernel 32-row x
+    // 64-column boxes (128-byte swizzle)
+    const bool smx = epilogue == GEMM_EPI_SOFTMAX;
+    if (!encode_2d(s.encode, &tc, C, static_cast<uint64_t>(N), static_cast<uint64_t>(M), smx ? 64 : 32, 32,
+                   smx ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
         return GEMM_ERR_LAUNCH;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The array keeps the previous call's contents: the error word must start at zero.

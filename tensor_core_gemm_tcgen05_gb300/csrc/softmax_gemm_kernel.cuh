@@ -55,15 +55,18 @@ struct SoftmaxConfig {
     // after the ring: barriers, TMEM address, stop flag; then each epilogue warp's 64 bias
     // values (FP16, 128 bytes)
     static constexpr int BIAS_OFFSET = STAGES * STAGE_BYTES + ((NUM_BARS * 8 + 16 + 15) / 16) * 16;
-    // then, 1024-aligned, two 32 x 32 FP16 output staging boxes per epilogue warp
+    // then, 1024-aligned, one 32 x 64 FP16 output staging box per epilogue warp (128-byte
+    // swizzle; C's tensor map has 64 x 32 boxes)
+    static constexpr int STORE_BOX_BYTES = 32 * WARP_COLS * 2;
     static constexpr int STORE_OFFSET = ((BIAS_OFFSET + NUM_EPI_WARPS * WARP_COLS * 2 + 1023) / 1024) * 1024;
     // then the column-group statistics: [2 buffers][4 quarters][4 groups][32 lanes] (max, sum)
-    static constexpr int GROUP_OFFSET = STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES;
+    static constexpr int GROUP_OFFSET = STORE_OFFSET + NUM_EPI_WARPS * STORE_BOX_BYTES;
     // then the cluster statistics of this CTA: [2 buffers][128 rows] (max, sum)
     static constexpr int CLUSTER_OFFSET = GROUP_OFFSET + 2 * 4 * GROUPS * 32 * 8;
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + CLUSTER_OFFSET + 2 * BM * 8;
 
-    static_assert(WARP_COLS == 64, "two 32-column chunks per epilogue warp");
+    static_assert(WARP_COLS == 64, "two 32-column chunks per epilogue warp, 128-byte output rows");
+    static_assert(STORE_BOX_BYTES % 1024 == 0, "128-byte-swizzled boxes start 1024-byte aligned");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 };
 
@@ -206,15 +209,16 @@ __device__ __forceinline__ bool wait_sleep(uint32_t bar, uint32_t parity, const 
     }
 }
 
-// Scale 32 FP32 values (SCALE) or take them as they are, round to FP16 and write them as
-// this thread's row of a 32 x 32 staging box (64-byte swizzle: 16-byte piece i of row r at
-// r*64 + (i ^ ((r >> 1) & 3))*16).
+// Scale 32 FP32 values (SCALE) or take them as they are, round to FP16 and write them as half
+// `h` (columns 32h..32h+31) of this thread's row of the warp's 32 x 64 staging box (128-byte
+// rows, 128-byte swizzle: 16-byte piece i of row r at r*128 + (i ^ (r & 7))*16, which also
+// spreads each quarter-warp's writes over all banks).
 template <bool SCALE>
-__device__ __forceinline__ void stage_row(const float *v, float scale, uint32_t box, int lane)
+__device__ __forceinline__ void stage_row(const float *v, float scale, uint32_t box, int h, int lane)
 {
     const uint64_t sc = f32x2_pack(scale, scale);
-    const uint32_t row_base = box + static_cast<uint32_t>(lane) * 64u;
-    const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+    const uint32_t row_base = box + static_cast<uint32_t>(lane) * 128u;
+    const uint32_t sw = static_cast<uint32_t>(lane & 7);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         uint32_t w[4];
@@ -227,11 +231,11 @@ __device__ __forceinline__ void stage_row(const float *v, float scale, uint32_t 
             __half2 hv = __floats2half2_rn(a, b);
             w[e] = *reinterpret_cast<uint32_t *>(&hv);
         }
-        st_shared_v4(row_base + ((static_cast<uint32_t>(i) ^ sw) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+        st_shared_v4(row_base + (((static_cast<uint32_t>(4 * h + i)) ^ sw) << 4), make_uint4(w[0], w[1], w[2], w[3]));
     }
 }
 
-// Before the warp refills its two staging boxes: the stores that last used them have read them.
+// Before the warp refills its staging box: the stores that last used them have read them.
 __device__ __forceinline__ void staging_free(int lane)
 {
     if (lane == 0)
@@ -239,16 +243,14 @@ __device__ __forceinline__ void staging_free(int lane)
     __syncwarp();
 }
 
-// Send the warp's two staged 32 x 32 boxes with TMA stores to columns n_first.. and
-// n_first + 32.., rows row0.. (the store clips rows >= M and columns >= N).
-__device__ __forceinline__ void store_boxes(uint32_t stage, const CUtensorMap *tmap_c, int n_first, int row0, int lane)
+// Send the warp's staged 32 x 64 box with one TMA store to columns n_first.., rows row0..
+// (the store clips rows >= M and columns >= N).
+__device__ __forceinline__ void store_box(uint32_t stage, const CUtensorMap *tmap_c, int n_first, int row0, int lane)
 {
     fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) {
-        const uint64_t pol = l2_policy_evict_first();
-        tma_store_2d(tmap_c, stage, n_first, row0, pol);
-        tma_store_2d(tmap_c, stage + EPI_STORE_BOX_BYTES, n_first + 32, row0, pol);
+        tma_store_2d(tmap_c, stage, n_first, row0, l2_policy_evict_first());
         bulk_commit_group();
     }
 }
@@ -501,7 +503,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int row = quarter * 32 + lane;       // this thread's row of the tile
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         uint4 *my_bias = bias_stage + ew * (Cfg::WARP_COLS / 8);
-        const uint32_t my_stage = base + Cfg::STORE_OFFSET + static_cast<uint32_t>(ew) * EPI_STORE_WARP_BYTES;
+        const uint32_t my_stage = base + Cfg::STORE_OFFSET + static_cast<uint32_t>(ew) * Cfg::STORE_BOX_BYTES;
         const uint32_t group_slots = base + Cfg::GROUP_OFFSET;
         const uint32_t my_group_bar = group0 + 8u * static_cast<uint32_t>(quarter);
         const bool has_acc = p.num_kb > 0;   // K = 0: the empty sum, no accumulator to read
@@ -594,9 +596,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 // m is the row maximum, s the row's sum of 2^(x log2(e) - m); v holds 2^(x log2(e) - mg)
                 const float scale = mg != -INFINITY ? ex2_approx(mg - m) * rcp_approx(s) : 0.0f;
                 staging_free(lane);
-                stage_row<true>(v, scale, my_stage, lane);
-                stage_row<true>(v + 32, scale, my_stage + EPI_STORE_BOX_BYTES, lane);
-                store_boxes(my_stage, &tmap_c, n_first, row0, lane);
+                stage_row<true>(v, scale, my_stage, 0, lane);
+                stage_row<true>(v + 32, scale, my_stage, 1, lane);
+                store_box(my_stage, &tmap_c, n_first, row0, lane);
             } else {
                 // pass 1: running row statistics over this CTA's tiles, 32 columns at a time
                 float m = -INFINITY, s = 0.0f;
@@ -650,9 +652,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         float v[32];
                         logits(r, sbias ? sbias + 4 * h : nullptr, n_first + 32 * h, p.N, v);
                         exp2_fma(v, off);
-                        stage_row<false>(v, 1.0f, my_stage + static_cast<uint32_t>(h) * EPI_STORE_BOX_BYTES, lane);
+                        stage_row<false>(v, 1.0f, my_stage, h, lane);
                     }
-                    store_boxes(my_stage, &tmap_c, n_first, row0, lane);
+                    store_box(my_stage, &tmap_c, n_first, row0, lane);
                 }
             }
         }
