@@ -536,6 +536,17 @@ int gemm_create(gemm_ctx **out, int device)
         delete ctx;
         return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);
     }
+    // The clock sampler shares an SM with the kernels it watches: with the default
+    // preference a CTA without shared memory may configure its SM for a small shared-memory
+    // carve-out, and no CTA needing 200+ KB can join that SM until it exits (a persistent
+    // GEMM then waits for it). Ask for the largest carve-out, the configuration the GEMM
+    // kernels use.
+    e = cudaFuncSetAttribute(gb300::clock_probe_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) {
+        delete ctx;
+        return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);
+    }
     // The pair kernel is used only if the device can co-schedule its clusters.
     if (cudaFuncSetAttribute(gb300::gemm_tcgen05_pair_kernel<PairCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              PairCfg::SMEM_BYTES) == cudaSuccess) {

@@ -188,22 +188,26 @@ __device__ __forceinline__ void merge_pairs(const float2 (&o)[N], float &m, floa
     s = S;
 }
 
-// Bounded wait for phase `parity` of `bar` that sleeps in the barrier instead of spinning:
-// the thread is suspended until the phase completes (or for at most about 20 us at a time,
-// after which the time limit and the other roles' stop flag are checked).
-__device__ __forceinline__ bool wait_sleep(uint32_t bar, uint32_t parity, const WaitCtl &w, uint32_t code)
+// Bounded wait for phase `parity` of `bar` by all 32 lanes of a warp together: every lane
+// polls (one warp-wide instruction, the same answer in every lane), so the warp stays
+// converged and needs no broadcast afterwards; lane 0 records a timeout. (Measured on
+// 262144 x 256 x 128, for the accumulator and column-group waits: 40.1 us with one lane
+// sleeping in the barrier and a shuffle, 36.8 us with this.)
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtl &w, uint32_t code, int lane)
 {
-    if (mbar_try_wait_sleep(bar, parity, 20000u))
+    if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u))
+        if (mbar_try_wait(bar, parity))
             return true;
         if (*w.abort)
             return false;
         if (global_timer_ns() - t0 > w.limit_ns) {
-            *w.abort = 1;
-            atomicCAS(w.err, 0u, code);
+            if (lane == 0) {
+                *w.abort = 1;
+                atomicCAS(w.err, 0u, code);
+            }
             return false;
         }
     }
@@ -267,12 +271,9 @@ __device__ __forceinline__ bool group_merge(uint32_t slots, uint32_t bar, uint32
     const uint32_t base = slots + ((buf * 4u + static_cast<uint32_t>(quarter)) * 4u * 32u) * 8u;
     st_shared_f2(base + (static_cast<uint32_t>(group) * 32u + static_cast<uint32_t>(lane)) * 8u, m, s);
     __syncwarp();
-    int ok = 1;
-    if (lane == 0) {
+    if (lane == 0)
         mbar_arrive(bar);   // release: the pairs above
-        ok = wait_sleep(bar, count & 1u, wc, ERR_ROW_EXCHANGE) ? 1 : 0;
-    }
-    if (!__shfl_sync(0xffffffffu, ok, 0))
+    if (!wait_warp(bar, count & 1u, wc, ERR_ROW_EXCHANGE, lane))
         return false;
     float2 o[4];
 #pragma unroll
@@ -518,10 +519,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             uint4 bv = make_uint4(0u, 0u, 0u, 0u);
             if (p.bias != nullptr && lane < 8 && n_first + 8 * lane < p.N)
                 bv = __ldg(reinterpret_cast<const uint4 *>(p.bias + n_first + 8 * lane));
-            int got = 1;
-            if (lane == 0)
-                got = wait_sleep(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
-            if (!__shfl_sync(0xffffffffu, got, 0))
+            if (!wait_warp(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR, lane))
                 return false;
             tc_fence_after_sync();
             if (p.bias != nullptr) {

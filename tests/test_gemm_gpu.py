@@ -188,12 +188,14 @@ def test_activation_accuracy_on_every_fp16_input(ctx):
 
 
 @pytest.mark.parametrize("shape", [(300, 256, 128), (129, 200, 64), (1000, 8, 512), (64, 64, 4096),
-                                   (4104, 256, 128), (5, 136, 8)], ids=lambda s: "x".join(map(str, s)))
+                                   (4104, 256, 128), (5, 136, 8), (300, 256, 192), (20000, 256, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("with_bias", [False, True])
 def test_softmax_epilogue(kctx, shape, with_bias):
-    """GEMM with the fused row softmax: within one FP16 ulp of the oracle's softmax of the
-    FP64 logits (the GPU's logits are FP32 sums; their error, about 1e-6 relative, moves a
-    probability by far less than an FP16 ulp)."""
+    """GEMM with the fused row softmax, rows of one tile: within one FP16 ulp of the oracle's
+    softmax of the FP64 logits (the GPU's logits are FP32 sums; their error, about 1e-6
+    relative, moves a probability by far less than an FP16 ulp). 20000 rows loop every CTA
+    over many tiles and ring phases."""
     M, N, K = shape
     A = inputs.random_fp16((M, K), 6000 + M, "normal")
     B = inputs.random_fp16((K, N), 6100 + N, "normal_inv_k", k=K)
