@@ -147,10 +147,7 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
     float m = -INFINITY, l = 0.0f;
     uint32_t va[32], vb[32];
     for (int j = 0; j < n_kv; ++j) {
-        int w = 1;
-        if (lane == 0)
-            w = wait_bounded(s_full, static_cast<uint32_t>(j) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
-        if (!__shfl_sync(0xffffffffu, w, 0))
+        if (!wait_warp(s_full, static_cast<uint32_t>(j) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR, lane))
             return;
         tc_fence_after_sync();
         const int k0 = j * Cfg::BKV;
@@ -202,9 +199,7 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
             const float alpha = raise ? ex2_approx(m - m_use) : 1.0f;   // 0 on the first block (m = -inf)
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
                 // P_t V of block j - 1 is pv_done's completion number j - 1
-                if (lane == 0)
-                    w = wait_bounded(pv_done, static_cast<uint32_t>(j - 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
-                if (!__shfl_sync(0xffffffffu, w, 0))
+                if (!wait_warp(pv_done, static_cast<uint32_t>(j - 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR, lane))
                     return false;
                 tc_fence_after_sync();
     #pragma unroll 1
@@ -283,10 +278,7 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
     }
     if (n_kv == 0)
         return;
-    int w = 1;
-    if (lane == 0)
-        w = wait_bounded(pv_done, static_cast<uint32_t>(n_kv - 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, w, 0))
+    if (!wait_warp(pv_done, static_cast<uint32_t>(n_kv - 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR, lane))
         return;
     tc_fence_after_sync();
     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
@@ -341,6 +333,12 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
     const int q0 = qb * Cfg::TILES * Cfg::BQ;
     const int k_end = p.causal ? min(p.Sk, q0 + Cfg::TILES * Cfg::BQ) : p.Sk;   // keys any row may see
     const int n_kv = (k_end + Cfg::BKV - 1) / Cfg::BKV;
+    // key blocks of tile t (causal: tile A's rows see no key past q0 + 127, so the block of
+    // keys q0 + 128 .. q0 + 255 is left out for it)
+    int n_t[Cfg::TILES];
+#pragma unroll
+    for (int t = 0; t < Cfg::TILES; ++t)
+        n_t[t] = p.causal ? min(n_kv, (min(p.Sk, q0 + (t + 1) * Cfg::BQ) + Cfg::BKV - 1) / Cfg::BKV) : n_kv;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -458,16 +456,16 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
                     issue_qk(1, 0);
                 }
             }
+            // block j of tile t exists for j < n_t[t] (n_t[0] <= n_t[1] = n_kv)
             for (int j = 0; ok && j < n_kv; ++j) {
-                const bool more = j + 1 < n_kv;
-                if (!issue_pv(0, j)) {
+                if (j < n_t[0] && !issue_pv(0, j)) {
                     ok = false;
                     break;
                 }
-                if (more) {
+                if (j + 1 < n_kv) {
                     const int s = (j + 1) & 1;
                     if (!wait_bounded(kv_full0 + 8u * s, static_cast<uint32_t>((j + 1) >> 1) & 1u, wc, ERR_MMA_OPERANDS) ||
-                        !next_qk(0, j)) {
+                        (j + 1 < n_t[0] && !next_qk(0, j))) {
                         ok = false;
                         break;
                     }
@@ -477,7 +475,7 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
                     break;
                 }
                 umma_commit(kv_empty0 + 8u * (j & 1));   // K_j and V_j consumed by both tiles
-                if (more && !next_qk(1, j)) {
+                if (j + 1 < n_t[1] && !next_qk(1, j)) {
                     ok = false;
                     break;
                 }
@@ -492,7 +490,7 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
         // ---------------------------------------------------------------- online softmax
         const int t = (warp - 2) >> 2;   // warps 2..5: tile A, 6..9: tile B
         attention_softmax_warp(p, tmem, t, s_full0 + 8u * t, p_half0 + 8u * t, p_full0 + 8u * t, pv_done0 + 8u * t, wc,
-                               warp, lane, q0 + t * Cfg::BQ, h, n_kv);
+                               warp, lane, q0 + t * Cfg::BQ, h, t == 0 ? n_t[0] : n_t[1]);
     }
 
     tc_fence_before_sync();

@@ -29,10 +29,13 @@ using Cfg = gb300::KernelConfig<128, 256, 4, GB300_EPI_WARPS>;
 #endif
 using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS>;
 // The same 128 x 256 tiles with a shorter ring and eight epilogue warps (two per TMEM lane
-// quarter, each with half of the columns): the whole-tile kernel when all tiles fit one
-// wave, where every CTA's epilogue is an exposed tail that twice the warps shorten (2048^3:
-// 15.6 -> 15.0 us).
+// quarter, each with half of the columns): the split-K instance.
 using Cfg8 = gb300::KernelConfig<128, 256, 3, 8>;
+// ... and with sixteen (four per lane quarter, 64 columns each, 96 registers): the whole-tile
+// kernel when all tiles fit one wave, where every CTA's epilogue is an exposed tail that more
+// warps shorten (2048^3 + bias + GELU, same box: 4 warps 18.6 us, 8 warps 18.0, 16 warps 17.3;
+// plain 15.6, 15.0, 15.0).
+using Cfg16 = gb300::KernelConfig<128, 256, 3, 16>;
 // The softmax epilogue's kernel: 128 x 256 tiles, 3-stage ring, sixteen epilogue warps.
 using SoftCfg = gb300::SoftmaxConfig<3>;
 // Split-K runs on the eight-warp instance: twice the warps to stage the partial and to
@@ -256,7 +259,7 @@ void launch_pdl_cluster(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, gb
 // The kernel instance gemm_run launches for a problem, with its grid and the schedule fields
 // of its parameters. make_plan decides; launch runs the plan; gemm_describe reports it.
 enum PlanKind : int {
-    PLAN_PAIR, PLAN_TILES, PLAN_TILES8, PLAN_STREAMK, PLAN_SPLITK, PLAN_ROWCLUSTER, PLAN_ROWCLUSTER2
+    PLAN_PAIR, PLAN_TILES, PLAN_TILES16, PLAN_STREAMK, PLAN_SPLITK, PLAN_ROWCLUSTER, PLAN_ROWCLUSTER2
 };
 
 struct Plan {
@@ -273,7 +276,7 @@ const char *plan_kernel_name(PlanKind k)
     switch (k) {
     case PLAN_PAIR: return "gemm_tcgen05_pair_kernel<PairConfig<256,6,4>>";
     case PLAN_TILES: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_TILES>";
-    case PLAN_TILES8: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,8>,SCHED_TILES>";
+    case PLAN_TILES16: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,16>,SCHED_TILES>";
     case PLAN_STREAMK: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_STREAM_K>";
     case PLAN_SPLITK: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,8>,SCHED_SPLIT_K>";
     case PLAN_ROWCLUSTER: return "gemm_softmax_kernel<SoftmaxConfig<3>,false>";
@@ -388,8 +391,8 @@ Plan make_plan(const gemm_ctx *ctx, int M, int N, int K, int epilogue)
             return pl;
         }
     }
-    // one wave: eight epilogue warps
-    pl.kind = pl.num_tiles <= ctx->num_sms ? PLAN_TILES8 : PLAN_TILES;
+    // one wave: sixteen epilogue warps
+    pl.kind = pl.num_tiles <= ctx->num_sms ? PLAN_TILES16 : PLAN_TILES;
     return pl;
 }
 
@@ -461,9 +464,9 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
         launch_pdl(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_STREAM_K>, pl.grid, Cfg::NUM_THREADS,
                    Cfg::SMEM_BYTES, stream, ta, tb, tc, p);
         break;
-    case PLAN_TILES8:
-        launch_pdl(gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_TILES>, pl.grid, Cfg8::NUM_THREADS,
-                   Cfg8::SMEM_BYTES, stream, ta, tb, tc, p);
+    case PLAN_TILES16:
+        launch_pdl(gb300::gemm_tcgen05_kernel<Cfg16, gb300::SCHED_TILES>, pl.grid, Cfg16::NUM_THREADS,
+                   Cfg16::SMEM_BYTES, stream, ta, tb, tc, p);
         break;
     case PLAN_TILES:
         launch_pdl(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_TILES>, pl.grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES,
@@ -524,8 +527,8 @@ int gemm_create(gemm_ctx **out, int device)
         e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg, gb300::SCHED_STREAM_K>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg8, gb300::SCHED_TILES>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg8::SMEM_BYTES);
+        e = cudaFuncSetAttribute(gb300::gemm_tcgen05_kernel<Cfg16, gb300::SCHED_TILES>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg16::SMEM_BYTES);
     if (e != cudaSuccess) {
         delete ctx;
         return cuda_fail(nullptr, e, GEMM_ERR_DEVICE);

@@ -188,31 +188,6 @@ __device__ __forceinline__ void merge_pairs(const float2 (&o)[N], float &m, floa
     s = S;
 }
 
-// Bounded wait for phase `parity` of `bar` by all 32 lanes of a warp together: every lane
-// polls (one warp-wide instruction, the same answer in every lane), so the warp stays
-// converged and needs no broadcast afterwards; lane 0 records a timeout. (Measured on
-// 262144 x 256 x 128, for the accumulator and column-group waits: 40.1 us with one lane
-// sleeping in the barrier and a shuffle, 36.8 us with this.)
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtl &w, uint32_t code, int lane)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if (*w.abort)
-            return false;
-        if (global_timer_ns() - t0 > w.limit_ns) {
-            if (lane == 0) {
-                *w.abort = 1;
-                atomicCAS(w.err, 0u, code);
-            }
-            return false;
-        }
-    }
-}
-
 // Scale 32 FP32 values (SCALE) or take them as they are, round to FP16 and write them as half
 // `h` (columns 32h..32h+31) of this thread's row of the warp's 32 x 64 staging box (128-byte
 // rows, 128-byte swizzle: 16-byte piece i of row r at r*128 + (i ^ (r & 7))*16, which also
