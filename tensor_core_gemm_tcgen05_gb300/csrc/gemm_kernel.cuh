@@ -919,10 +919,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             int t, mb, nb, k0, k1;
             while (work.next(p, t, mb, nb, k0, k1)) {
                 const uint4 bv = bias_fetch(p, nb * BN, lane);
-                int ok = 1;
-                if (lane == 0)
-                    ok = wait_bounded(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR) ? 1 : 0;
-                ok = __shfl_sync(0xffffffffu, ok, 0);
+                // all lanes poll (see wait_warp): fewer issue slots taken from the producer and
+                // MMA threads than one lane spinning (2048^3 at the power limit: 19.4 -> 18.6 us)
+                int ok = wait_warp(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR, lane) ? 1 : 0;
                 if (!ok)
                     break;
                 tc_fence_after_sync();
