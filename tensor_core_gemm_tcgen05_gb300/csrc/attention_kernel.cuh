@@ -47,7 +47,6 @@ struct AttnParams {
     int q_blocks;       // ceil(Sq / 256): CTAs per head
     int causal;
     float scale_log2;   // scale * log2(e): scores are kept in base-2 units
-    __half *O;          // [H][Sq][128]
     uint32_t *err;
     uint64_t timeout_ns;
 };
@@ -131,9 +130,13 @@ __device__ __forceinline__ void two_buffered_chunks(uint32_t addr, uint32_t (&va
 // the first 64 score columns (chunk c of 32 keys to columns 16c..16c+15: each lies in score
 // columns that were already read), summing p into the running denominator l. At the end the
 // row of O is divided by l and stored.
+//
+// `o_stage`: the tile's Q buffer in shared memory, free once its last S product has
+// completed, where the rows of O are staged for the TMA store (`tmap_o`).
 __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint32_t tmem, int tile, uint32_t s_full,
                                                        uint32_t p_half, uint32_t p_full, uint32_t pv_done,
-                                                       const WaitCtl &wc, int warp, int lane, int q0, int h, int n_kv)
+                                                       const WaitCtl &wc, int warp, int lane, int q0, int h, int n_kv,
+                                                       uint32_t o_stage, const CUtensorMap *tmap_o)
 {
     using Cfg = AttnConfig;
     const int quarter = warp & 3;
@@ -282,30 +285,46 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
         return;
     tc_fence_after_sync();
     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-    __half *orow = p.O + (static_cast<int64_t>(h) * p.Sq + qi) * Cfg::D;
+    // The warp's 32 rows of O / l, rounded to FP16, staged as two 64-column boxes of 32 rows
+    // (128-byte swizzle: 16-byte piece k of row r at piece k ^ (r mod 8)), then written by two
+    // TMA stores, which clip rows past the sequence. The last S product of the tile, which
+    // read the buffer, completed before pv_done's last phase.
+    const uint32_t row_base = o_stage + static_cast<uint32_t>(quarter) * 4096u + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
         tmem_ld_32x32b_x32(o_addr + 32u * c, va);
         tmem_ld_wait_regs(va);
-        if (qi < p.Sq) {
+        const uint32_t row = row_base + static_cast<uint32_t>(c >> 1) * Cfg::ATOM_BYTES;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t pk[4];
+        for (int i = 0; i < 4; ++i) {
+            uint32_t pk[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    __half2 hh = __floats2half2_rn(__uint_as_float(va[8 * i + 2 * e]) * inv,
-                                                   __uint_as_float(va[8 * i + 2 * e + 1]) * inv);
-                    pk[e] = *reinterpret_cast<uint32_t *>(&hh);
-                }
-                *reinterpret_cast<uint4 *>(orow + 32 * c + 8 * i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int e = 0; e < 4; ++e) {
+                __half2 hh = __floats2half2_rn(__uint_as_float(va[8 * i + 2 * e]) * inv,
+                                               __uint_as_float(va[8 * i + 2 * e + 1]) * inv);
+                pk[e] = *reinterpret_cast<uint32_t *>(&hh);
             }
+            const uint32_t piece = static_cast<uint32_t>(((c & 1) * 4 + i) ^ (lane & 7));
+            st_shared_v4(row + piece * 16u, make_uint4(pk[0], pk[1], pk[2], pk[3]));
         }
     }
+    fence_proxy_async_shared();
+    __syncwarp();
+    const int row0 = q0 + quarter * 32;
+    if (lane == 0 && row0 < p.Sq) {
+        for (int a = 0; a < 2; ++a)
+            tma_store_3d(tmap_o, o_stage + static_cast<uint32_t>(a) * Cfg::ATOM_BYTES + static_cast<uint32_t>(quarter) * 4096u,
+                         64 * a, row0, h);
+        bulk_commit_group();
+        bulk_wait_group<0>();   // the stores have read shared memory and written O before the CTA ends
+    }
+    __syncwarp();
 }
 
 __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
     attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                         const __grid_constant__ CUtensorMap tmap_v, const AttnParams p)
+                         const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
+                         const AttnParams p)
 {
     using Cfg = AttnConfig;
     constexpr uint32_t ATOM = Cfg::ATOM_BYTES, TILE = Cfg::TILE_BYTES;
@@ -358,6 +377,7 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
+        tma_prefetch_desc(&tmap_o);
     }
     if (warp == 1) {
         tmem_alloc<1>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -412,19 +432,23 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
             constexpr uint32_t ID_QK = idesc_attn<false>(), ID_PV = idesc_attn<true>();
             bool ok = wait_bounded(q_full, 0, wc, ERR_MMA_OPERANDS);
             // S_t = Q_t K_j^T into tile t's score columns
+            const uint64_t q_desc0 = kmajor_step_desc(sQ, 0), k_desc0 = kmajor_step_desc(sKV, 0),
+                           v_desc0 = v_step_desc(sKV + TILE, 0);
             auto issue_qk = [&](int t, int j) {
-                const uint32_t sK = sKV + static_cast<uint32_t>(j & 1) * 2u * TILE;
+                const uint64_t qd = q_desc0 + static_cast<uint64_t>(t * (TILE >> 4));
+                const uint64_t kd = k_desc0 + static_cast<uint64_t>((j & 1) * (2 * TILE >> 4));
                 const uint32_t d = tmem + static_cast<uint32_t>(Cfg::S_COL + t * Cfg::BQ);
 #pragma unroll
-                for (int kk = 0; kk < Cfg::D / 16; ++kk)
-                    umma_f16<1>(d, kmajor_step_desc(sQ + t * TILE, kk), kmajor_step_desc(sK, kk), ID_QK,
-                                kk != 0 ? 1u : 0u);
+                for (int kk = 0; kk < Cfg::D / 16; ++kk) {
+                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * Cfg::ATOM_BYTES + (kk & 3) * 32) >> 4);
+                    umma_f16<1>(d, qd + off, kd + off, ID_QK, kk != 0 ? 1u : 0u);
+                }
                 umma_commit(s_full0 + 8u * t);
             };
             // O_t += P_t V_j, P_t from TMEM (8 columns per 16 keys)
             // (keys 0..63 as soon as their P is written, keys 64..127 once all of it is)
             auto issue_pv = [&](int t, int j) -> bool {
-                const uint32_t sV = sKV + static_cast<uint32_t>(j & 1) * 2u * TILE + TILE;
+                const uint64_t vd = v_desc0 + static_cast<uint64_t>((j & 1) * (2 * TILE >> 4));
                 const uint32_t d = tmem + static_cast<uint32_t>(Cfg::O_COL + t * Cfg::D);
                 const uint32_t a = tmem + static_cast<uint32_t>(Cfg::S_COL + t * Cfg::BQ);
                 for (int part = 0; part < 2; ++part) {
@@ -434,7 +458,7 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
                     tc_fence_after_sync();
 #pragma unroll
                     for (int kk = 4 * part; kk < 4 * part + 4; ++kk)
-                        umma_f16_tmem_a(d, a + 8u * static_cast<uint32_t>(kk), v_step_desc(sV, kk), ID_PV,
+                        umma_f16_tmem_a(d, a + 8u * static_cast<uint32_t>(kk), vd + static_cast<uint64_t>(kk * (2048 >> 4)), ID_PV,
                                         (j | kk) != 0 ? 1u : 0u);
                 }
                 umma_commit(pv_done0 + 8u * t);
@@ -490,7 +514,7 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
         // ---------------------------------------------------------------- online softmax
         const int t = (warp - 2) >> 2;   // warps 2..5: tile A, 6..9: tile B
         attention_softmax_warp(p, tmem, t, s_full0 + 8u * t, p_half0 + 8u * t, p_full0 + 8u * t, pv_done0 + 8u * t, wc,
-                               warp, lane, q0 + t * Cfg::BQ, h, t == 0 ? n_t[0] : n_t[1]);
+                               warp, lane, q0 + t * Cfg::BQ, h, t == 0 ? n_t[0] : n_t[1], sQ + t * TILE, &tmap_o);
     }
 
     tc_fence_before_sync();

@@ -954,7 +954,7 @@ int gemm_attention_fwd(gemm_ctx *ctx, int64_t heads, int64_t seq_q, int64_t seq_
         return GEMM_ERR_DEVICE;
     DeviceGuard guard(ctx->device);
     // [head][row][dim] views, boxes of 64 dims (one 128-byte swizzle row) x box_rows rows:
-    // 128 query rows (a query tile), 64 key rows (a key block)
+    // 128 query rows (a query tile), 128 key rows (a key block)
     auto encode_3d = [&](CUtensorMap *map, const void *ptr, int64_t rows, uint32_t box_rows) {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(Cfg::D), static_cast<cuuint64_t>(rows),
                                     static_cast<cuuint64_t>(heads)};
@@ -965,9 +965,10 @@ int gemm_attention_fwd(gemm_ctx *ctx, int64_t heads, int64_t seq_q, int64_t seq_
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    CUtensorMap tq, tk, tv;
+    // O: stores of 32 rows (one softmax warp's share of a query tile)
+    CUtensorMap tq, tk, tv, to;
     if (!encode_3d(&tq, Q, seq_q, Cfg::BQ) || !encode_3d(&tk, K, seq_k, Cfg::BKV) ||
-        !encode_3d(&tv, V, seq_k, Cfg::BKV))
+        !encode_3d(&tv, V, seq_k, Cfg::BKV) || !encode_3d(&to, O, seq_q, 32))
         return GEMM_ERR_LAUNCH;
     gb300::AttnParams p;
     p.H = static_cast<int>(heads);
@@ -976,7 +977,6 @@ int gemm_attention_fwd(gemm_ctx *ctx, int64_t heads, int64_t seq_q, int64_t seq_
     p.q_blocks = static_cast<int>(q_blocks);
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.O = static_cast<__half *>(O);
     p.err = ctx->d_err;
     p.timeout_ns = ctx->timeout_ns;
     cudaLaunchConfig_t cfg = {};
@@ -989,7 +989,7 @@ int gemm_attention_fwd(gemm_ctx *ctx, int64_t heads, int64_t seq_q, int64_t seq_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaLaunchKernelEx(&cfg, gb300::attention_fwd_kernel, tq, tk, tv, p);
+    cudaLaunchKernelEx(&cfg, gb300::attention_fwd_kernel, tq, tk, tv, to, p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GEMM_OK : cuda_fail(ctx, e, GEMM_ERR_LAUNCH);
 }

@@ -228,6 +228,15 @@ __device__ __forceinline__ void tma_store_2d(const void *map, uint32_t src, int3
                  : "memory");
 }
 
+// 3-D tiled store of a box from shared memory (no L2 hint).
+__device__ __forceinline__ void tma_store_3d(const void *map, uint32_t src, int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");

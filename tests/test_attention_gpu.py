@@ -133,6 +133,38 @@ def test_attention_full_size_every_head(ctx, causal):
     assert worst < 3e-3
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,Sq,Sk", [(200, 256, 256), (160, 300, 700), (170, 520, 130), (4, 8192, 8192)],
+                         ids=lambda v: str(v))
+def test_attention_several_items_per_cta(ctx, H, Sq, Sk, causal):
+    """More work items (a head and a block of 256 queries) than SMs: each CTA of the
+    persistent grid runs several items in turn, and when causal their key counts differ from
+    one item to the next. Every row against plain FP32 PyTorch on the GPU, sampled rows of
+    every head against the FP64 oracle, same elementwise bar."""
+    Q, K, V = qkv(H, Sq, Sk, 3 * H + Sq + Sk)
+    scale = 0.09
+    O = run(ctx, Q, K, V, scale, causal)
+    rows = [(h, int(i)) for h in range(H) for i in inputs.sample_rows(Sq, 6, seed=h, include_last=1)]
+    ref, _ = oracle.attention(Q, K, V, scale, causal, rows=rows)
+    check(np.stack([O[h, i].numpy() for h, i in rows]), ref, f"H={H} Sq={Sq} Sk={Sk} causal={causal}")
+    dev = torch.device("cuda:0")
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        # query i sees keys 0 .. min(i, Sk - 1) when causal
+        mask = (torch.arange(Sk, device=dev)[None, :] <= torch.arange(Sq, device=dev)[:, None]) if causal else None
+        for h in range(H):
+            s_ = (Q[h].to(dev).float() @ K[h].to(dev).float().T) * scale
+            if mask is not None:
+                s_ = s_.masked_fill(~mask, float("-inf"))
+            ref_h = torch.softmax(s_, dim=1) @ V[h].to(dev).float()
+            err = (O[h].to(dev).float() - ref_h).abs()
+            bad = err > 3e-3 + 4e-3 * ref_h.abs()
+            assert not bool(bad.any()), (h, int(bad.sum()), float(err.max()))
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
 def test_attention_special_cases(ctx):
     H, S = 2, 384
     _, K, V = qkv(H, S, S, 31)
