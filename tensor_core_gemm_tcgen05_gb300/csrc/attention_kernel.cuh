@@ -10,8 +10,8 @@
 // per block; "Designing High-Performance GPU Kernels with TileLang" on spaxe.top: causal and
 // non-causal). Built on the same fifth-generation tensor-core machinery as the GEMM:
 //
-//  * one CTA per (head, block of 256 queries) = two query tiles A and B of 128 rows; the
-//    blocks with the most keys (causal) start first;
+//  * one CTA per (head, block of 256 queries) = two query tiles A and B of 128 rows; heads in
+//    groups of eight, within a group the blocks with the most keys (causal) first;
 //  * warp 0: TMA producer. Both Q tiles once (K-major, two 128-byte-swizzled atoms of 64 head
 //    dims each), then K and V blocks of 128 keys through a two-stage ring; 3-D tensor maps
 //    [head][row][dim] so that rows past the sequence read as zero;
@@ -40,6 +40,9 @@ namespace gb300 {
 // exceeds it by more than this many base-2 units; otherwise probabilities are taken against
 // the old maximum and stay below 2^8, well inside FP16 and FP32.
 constexpr float kRescaleThreshold = 8.0f;
+
+// Heads per group in the order of the work items (see the kernel).
+constexpr int kAttnHeadGroup = 8;
 
 struct AttnParams {
     int H;              // heads (batch x heads)
@@ -345,10 +348,16 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // work item: query block qb (256 queries, two tiles) of head h; the blocks with the most
-    // keys go first
-    const int qb = p.q_blocks - 1 - static_cast<int>(blockIdx.x / static_cast<unsigned>(p.H));
-    const int h = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.H));
+    // work item: query block qb (256 queries, two tiles) of head h. Heads are taken in groups
+    // of kAttnHeadGroup; within a group the blocks with the most keys (causal) go first, heads
+    // fastest. The CTAs in flight then share the keys and values of a few heads in L2 (64 x
+    // 4096 full: +8 % against all heads at once) and, when causal, the long items still start
+    // before the short ones.
+    const int grp = static_cast<int>(blockIdx.x) / (kAttnHeadGroup * p.q_blocks);
+    const int r = static_cast<int>(blockIdx.x) % (kAttnHeadGroup * p.q_blocks);
+    const int heads_in_grp = min(kAttnHeadGroup, p.H - grp * kAttnHeadGroup);
+    const int qb = p.q_blocks - 1 - r / heads_in_grp;
+    const int h = grp * kAttnHeadGroup + r % heads_in_grp;
     const int q0 = qb * Cfg::TILES * Cfg::BQ;
     const int k_end = p.causal ? min(p.Sk, q0 + Cfg::TILES * Cfg::BQ) : p.Sk;   // keys any row may see
     const int n_kv = (k_end + Cfg::BKV - 1) / Cfg::BKV;
