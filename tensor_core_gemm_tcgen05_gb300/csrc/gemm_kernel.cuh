@@ -832,6 +832,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            // Shared-memory descriptors of stage 0's A and B; every other step is a constant
+            // offset in the start-address field (16-byte units; addresses stay below 256 KB, so
+            // the 14-bit field never carries). A, K-major: the next 16 K-values are 32 bytes
+            // further along each 128-byte swizzled row, 8-row groups 1024 bytes apart. B,
+            // MN-major: 16 K-rows are 2048 bytes further, 8-row K groups 1024 bytes apart (SBO),
+            // 64-column N atoms one box apart (LBO).
+            const uint64_t a_desc0 = sw128_desc(sA, 16, 1024), b_desc0 = sw128_desc(sB, Cfg::B_BOX_BYTES, 1024);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
@@ -850,18 +857,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA + stage * Cfg::A_BYTES;
-                    const uint32_t b0 = sB + stage * Cfg::B_BYTES;
+                    const uint64_t a_st = a_desc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
+                    const uint64_t b_st = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk) {
-                        // A, K-major: the next 16 K-values are 32 bytes further along each
-                        // 128-byte swizzled row; 8-row groups are 1024 bytes apart.
-                        const uint64_t adesc = sw128_desc(a0 + kk * 32, 16, 1024);
-                        // B, MN-major: 16 K-rows are 2048 bytes further; 8-row K groups are
-                        // 1024 bytes apart (SBO); 64-column N atoms are one box apart (LBO).
-                        const uint64_t bdesc = sw128_desc(b0 + kk * 2048, Cfg::B_BOX_BYTES, 1024);
-                        umma_f16<1>(d_tmem, adesc, bdesc, IDESC, (kb != k0 || kk != 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk)
+                        umma_f16<1>(d_tmem, a_st + static_cast<uint64_t>(2 * kk), b_st + static_cast<uint64_t>(128 * kk), IDESC,
+                                    (kb != k0 || kk != 0) ? 1u : 0u);
                     umma_commit(empty0 + 8u * stage);   // slot free once these MMAs have read it
                     if (++stage == STAGES) {
                         stage = 0;

@@ -233,6 +233,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (CTA 0 only)
         if (leader && lane == 0) {
+            // descriptors of stage 0's A and B; steps are constant offsets in the start-address
+            // field (A: 32 bytes per 16 K-values, B: 2048 bytes per 16 K-rows; one stage apart)
+            const uint64_t a_desc0 = sw128_desc(sA, 16, 1024), b_desc0 = sw128_desc(sB, Cfg::B_BOX_BYTES, 1024);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
@@ -249,14 +252,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA + stage * Cfg::A_BYTES;
-                    const uint32_t b0 = sB + stage * Cfg::B_BYTES;
+                    const uint64_t a_st = a_desc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
+                    const uint64_t b_st = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk) {
-                        const uint64_t adesc = sw128_desc(a0 + kk * 32, 16, 1024);
-                        const uint64_t bdesc = sw128_desc(b0 + kk * 2048, Cfg::B_BOX_BYTES, 1024);
-                        umma_f16<2>(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk)
+                        umma_f16<2>(d_tmem, a_st + static_cast<uint64_t>(2 * kk), b_st + static_cast<uint64_t>(128 * kk), IDESC,
+                                    (kb | kk) != 0 ? 1u : 0u);
                     umma_commit_pair(empty0 + 8u * stage, 0x3);   // both CTAs' slots are free
                     if (++stage == STAGES) {
                         stage = 0;
