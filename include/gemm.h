@@ -46,13 +46,14 @@ enum gemm_epilogue {
     GEMM_EPI_GELU = 1, /* C = GELU_erf(A*B (+ bias))                                 */
     GEMM_EPI_RELU = 2, /* C = max(A*B (+ bias), 0)                                   */
     GEMM_EPI_SOFTMAX = 3 /* C[r][:] = softmax over the row of A*B (+ bias): the logits stay
-                            in FP32 inside the kernel and are never written. N <= 256:
-                            one tile spans the row. 256 < N <= 4096: a thread-block
-                            cluster of ceil(N/256) CTAs spans it and merges per-CTA row
-                            maxima and sums through distributed shared memory (cluster
-                            sizes above 8 need the device to schedule them; a width it
-                            cannot schedule, or N > 4096, returns GEMM_ERR_ARG: run
-                            GEMM_EPI_NONE, then gemm_row_softmax).
+                            in FP32 inside the kernel and are never written. Any N.
+                            N <= 256: one 128 x 256 tile spans the row, one pass. Wider
+                            rows: a thread-block cluster of 1, 2, 4 or 8 CTAs per block of
+                            128 rows, each CTA a span of 256-column tiles, two passes
+                            (running row maximum and sum over the span, merged across
+                            the cluster through distributed shared memory; then the
+                            logits are recomputed and the probabilities written). Returns
+                            GEMM_ERR_ARG only if the device cannot run the kernel at all.
                             "Designing High-Performance GPU Kernels with TileLang"
                             (spaxe.top): row-wise softmax in the GEMM epilogue.       */
 };
