@@ -25,9 +25,12 @@ namespace {
 #endif
 using Cfg = gb300::KernelConfig<128, 256, 4, GB300_EPI_WARPS>;
 #ifndef GB300_PAIR_STAGES
-#define GB300_PAIR_STAGES 6
+#define GB300_PAIR_STAGES 3
 #endif
-using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS>;
+#ifndef GB300_PAIR_BK
+#define GB300_PAIR_BK 128
+#endif
+using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS, GB300_PAIR_BK>;
 // The same 128 x 256 tiles with a shorter ring and eight epilogue warps (two per TMEM lane
 // quarter, each with half of the columns): the split-K instance.
 using Cfg8 = gb300::KernelConfig<128, 256, 3, 8>;
@@ -274,7 +277,7 @@ struct Plan {
 const char *plan_kernel_name(PlanKind k)
 {
     switch (k) {
-    case PLAN_PAIR: return "gemm_tcgen05_pair_kernel<PairConfig<256,6,4>>";
+    case PLAN_PAIR: return "gemm_tcgen05_pair_kernel<PairConfig<256,3,4,128>>";
     case PLAN_TILES: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_TILES>";
     case PLAN_TILES16: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,16>,SCHED_TILES>";
     case PLAN_STREAMK: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_STREAM_K>";
@@ -404,13 +407,16 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     CUtensorMap ta, tb, tc;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
+    const Plan pl = make_plan(ctx, M, N, K, epilogue);
+    // K per ring stage of the chosen kernel: A goes in 64-wide boxes either way, B in boxes
+    // of that many rows
+    const int bk = pl.kind == PLAN_PAIR ? PairCfg::BK : Cfg::BK;
     if (K > 0) {
         if (!encode_2d(ctx, &ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), Cfg::BK, Cfg::BM) ||
-            !encode_2d(ctx, &tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), Cfg::B_BOX_N, Cfg::BK,
-                       CU_TENSOR_MAP_SWIZZLE_128B, static_cast<uint64_t>(ldb)))
+            !encode_2d(ctx, &tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), Cfg::B_BOX_N,
+                       static_cast<uint32_t>(bk), CU_TENSOR_MAP_SWIZZLE_128B, static_cast<uint64_t>(ldb)))
             return GEMM_ERR_LAUNCH;
     }
-    const Plan pl = make_plan(ctx, M, N, K, epilogue);
     // C is written by TMA in 32 x 32 boxes staged with the 64-byte swizzle; the softmax
     // kernel writes 32-row x 64-column boxes staged with the 128-byte swizzle
     const bool smx = pl.kind == PLAN_ROWCLUSTER || pl.kind == PLAN_ROWCLUSTER2;
@@ -421,7 +427,7 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     p.M = M;
     p.N = N;
     p.K = K;
-    p.num_kb = (K + Cfg::BK - 1) / Cfg::BK;
+    p.num_kb = (K + bk - 1) / bk;
     p.epilogue = epilogue;
     p.bias = static_cast<const __half *>(bias);
     p.C = static_cast<__half *>(C);

@@ -23,13 +23,18 @@
 
 namespace gb300 {
 
-template <int BN_, int STAGES_, int EPI_WARPS_ = 4>
+template <int BN_, int STAGES_, int EPI_WARPS_ = 4, int BK_ = 64>
 struct PairConfig {
     static constexpr int CTA_BM = 128;     // rows per CTA (= TMEM lanes)
     static constexpr int BM = 256;         // rows per pair tile (= UMMA M)
     static constexpr int BN = BN_;         // columns per tile (= UMMA N)
     static constexpr int CTA_BN = BN / 2;  // B columns staged by each CTA
-    static constexpr int BK = 64;
+    // K per ring stage: one or two 64-wide 128-byte swizzle atoms of A (16 KB each per CTA).
+    // The MMA thread commits the stage's empty barrier once per stage, and each commit holds
+    // the tensor pipe for about 40 cycles, so wider stages issue fewer of them.
+    static constexpr int BK = BK_;
+    static constexpr int A_ATOM_BYTES = CTA_BM * 64 * 2;
+    static constexpr int A_ATOMS = BK / 64;
     static constexpr int UMMA_K = 16;
     static constexpr int STAGES = STAGES_;
     static constexpr int A_BYTES = CTA_BM * BK * 2;
@@ -49,6 +54,7 @@ struct PairConfig {
     static constexpr int SMEM_BYTES = 1024 + STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES;
 
     static_assert(BN % 128 == 0 && BN >= 128 && BN <= 256, "UMMA N for M = 256, two 64-column boxes per CTA");
+    static_assert(BK == 64 || BK == 128, "one or two A atoms per stage; B boxes BK rows tall");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM alloc size");
     static_assert(NUM_EPI_WARPS == 4 || NUM_EPI_WARPS == 8, "one or two warps per TMEM lane quarter");
     static_assert((BN / 32) % EPI_COL_GROUPS == 0, "column chunks split evenly between warps");
@@ -201,8 +207,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
                         const uint32_t fb = full0_leader + 8u * stage;
                         if (leader)   // CTA 0's barrier counts the bytes of both CTAs
                             mbar_arrive_expect_tx(full0 + 8u * stage, 2 * Cfg::STAGE_BYTES);
-                        tma_load_2d_pair(sA + stage * Cfg::A_BYTES, &tmap_a, fb, kb * BK,
-                                         mb * BM + static_cast<int>(rank) * Cfg::CTA_BM);
+#pragma unroll
+                        for (int a = 0; a < Cfg::A_ATOMS; ++a)
+                            tma_load_2d_pair(sA + stage * Cfg::A_BYTES + a * Cfg::A_ATOM_BYTES, &tmap_a, fb,
+                                             kb * BK + 64 * a, mb * BM + static_cast<int>(rank) * Cfg::CTA_BM);
 #pragma unroll
                         for (int j = 0; j < Cfg::B_BOXES; ++j)
                             tma_load_2d_pair(sB + stage * Cfg::B_BYTES + j * Cfg::B_BOX_BYTES, &tmap_b, fb,
@@ -234,7 +242,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
         // ------------------------------------------------------------ MMA issuer (CTA 0 only)
         if (leader && lane == 0) {
             // descriptors of stage 0's A and B; steps are constant offsets in the start-address
-            // field (A: 32 bytes per 16 K-values, B: 2048 bytes per 16 K-rows; one stage apart)
+            // field (A: 32 bytes per 16 K-values within a 64-wide atom, the next atom 16 KB on;
+            // B: 2048 bytes per 16 K-rows; one stage apart)
             const uint64_t a_desc0 = sw128_desc(sA, 16, 1024), b_desc0 = sw128_desc(sB, Cfg::B_BOX_BYTES, 1024);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
@@ -256,8 +265,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
                     const uint64_t b_st = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
 #pragma unroll
                     for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk)
-                        umma_f16<2>(d_tmem, a_st + static_cast<uint64_t>(2 * kk), b_st + static_cast<uint64_t>(128 * kk), IDESC,
-                                    (kb | kk) != 0 ? 1u : 0u);
+                        umma_f16<2>(d_tmem,
+                                    a_st + static_cast<uint64_t>((kk >> 2) * (Cfg::A_ATOM_BYTES >> 4) + 2 * (kk & 3)),
+                                    b_st + static_cast<uint64_t>(128 * kk), IDESC, (kb | kk) != 0 ? 1u : 0u);
                     umma_commit_pair(empty0 + 8u * stage, 0x3);   // both CTAs' slots are free
                     if (++stage == STAGES) {
                         stage = 0;
