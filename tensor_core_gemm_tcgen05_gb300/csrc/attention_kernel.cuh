@@ -136,11 +136,19 @@ __device__ __forceinline__ void two_buffered_chunks(uint32_t addr, uint32_t (&va
 //
 // `o_stage`: the tile's Q buffer in shared memory, free once its last S product has
 // completed, where the rows of O are staged for the TMA store (`tmap_o`).
+// The completion of the tile's P V product of block b: with `pv_per_stage` false, phase b of
+// the barrier `pv_done`; with it true (tile B), phase b / 2 of barrier b mod 2 of the pair at
+// `pv_done` (the key/value ring's empty barriers, which tile B's P V products complete).
 __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint32_t tmem, int tile, uint32_t s_full,
                                                        uint32_t p_half, uint32_t p_full, uint32_t pv_done,
                                                        const WaitCtl &wc, int warp, int lane, int q0, int h, int n_kv,
-                                                       uint32_t o_stage, const CUtensorMap *tmap_o)
+                                                       uint32_t o_stage, const CUtensorMap *tmap_o, bool pv_per_stage)
 {
+    auto wait_pv = [&](int b) -> bool {
+        const uint32_t ub = static_cast<uint32_t>(b);
+        return pv_per_stage ? wait_warp(pv_done + 8u * (ub & 1u), (ub >> 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR, lane)
+                            : wait_warp(pv_done, ub & 1u, wc, ERR_EPILOGUE_ACCUMULATOR, lane);
+    };
     using Cfg = AttnConfig;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
@@ -204,8 +212,7 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
             const float m_use = m_new == -INFINITY ? 0.0f : m_new;
             const float alpha = raise ? ex2_approx(m - m_use) : 1.0f;   // 0 on the first block (m = -inf)
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-                // P_t V of block j - 1 is pv_done's completion number j - 1
-                if (!wait_warp(pv_done, static_cast<uint32_t>(j - 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR, lane))
+                if (!wait_pv(j - 1))   // P_t V of block j - 1 done
                     return false;
                 tc_fence_after_sync();
     #pragma unroll 1
@@ -284,7 +291,7 @@ __device__ __forceinline__ void attention_softmax_warp(const AttnParams &p, uint
     }
     if (n_kv == 0)
         return;
-    if (!wait_warp(pv_done, static_cast<uint32_t>(n_kv - 1) & 1u, wc, ERR_EPILOGUE_ACCUMULATOR, lane))
+    if (!wait_pv(n_kv - 1))
         return;
     tc_fence_after_sync();
     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
@@ -470,12 +477,18 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
                         umma_f16_tmem_a(d, a + 8u * static_cast<uint32_t>(kk), vd + static_cast<uint64_t>(kk * (2048 >> 4)), ID_PV,
                                         (j | kk) != 0 ? 1u : 0u);
                 }
-                umma_commit(pv_done0 + 8u * t);
+                // Tile A's product completes pv_done[0]; tile B's is followed at once by the
+                // commit that frees the key/value stage, whose completion serves for it too (one
+                // commit fewer per block: each holds the tensor pipe for about 40 cycles).
+                if (t == 0)
+                    umma_commit(pv_done0);
                 return true;
             };
             // the next S_t overwrites P_t: only once this tile's P V product has finished
             auto next_qk = [&](int t, int j) -> bool {
-                if (!wait_bounded(pv_done0 + 8u * t, static_cast<uint32_t>(j) & 1u, wc, ERR_MMA_ACCUMULATOR))
+                const uint32_t uj = static_cast<uint32_t>(j);
+                if (!(t == 0 ? wait_bounded(pv_done0, uj & 1u, wc, ERR_MMA_ACCUMULATOR)
+                             : wait_bounded(kv_empty0 + 8u * (uj & 1u), (uj >> 1) & 1u, wc, ERR_MMA_ACCUMULATOR)))
                     return false;
                 tc_fence_after_sync();
                 issue_qk(t, j + 1);
@@ -522,8 +535,9 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
     } else {
         // ---------------------------------------------------------------- online softmax
         const int t = (warp - 2) >> 2;   // warps 2..5: tile A, 6..9: tile B
-        attention_softmax_warp(p, tmem, t, s_full0 + 8u * t, p_half0 + 8u * t, p_full0 + 8u * t, pv_done0 + 8u * t, wc,
-                               warp, lane, q0 + t * Cfg::BQ, h, t == 0 ? n_t[0] : n_t[1], sQ + t * TILE, &tmap_o);
+        attention_softmax_warp(p, tmem, t, s_full0 + 8u * t, p_half0 + 8u * t, p_full0 + 8u * t,
+                               t == 0 ? pv_done0 : kv_empty0, wc, warp, lane, q0 + t * Cfg::BQ, h,
+                               t == 0 ? n_t[0] : n_t[1], sQ + t * TILE, &tmap_o, t != 0);
     }
 
     tc_fence_before_sync();
