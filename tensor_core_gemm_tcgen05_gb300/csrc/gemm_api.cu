@@ -31,20 +31,23 @@ using Cfg = gb300::KernelConfig<128, 256, 4, GB300_EPI_WARPS>;
 #define GB300_PAIR_BK 128
 #endif
 using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS, GB300_PAIR_BK>;
-// The same 128 x 256 tiles with a shorter ring and eight epilogue warps (two per TMEM lane
-// quarter, each with half of the columns): the split-K instance.
-using Cfg8 = gb300::KernelConfig<128, 256, 3, 8>;
-// ... and with sixteen (four per lane quarter, 64 columns each, 96 registers): the whole-tile
-// kernel when all tiles fit one wave, where every CTA's epilogue is an exposed tail that more
-// warps shorten (2048^3 + bias + GELU, same box: 4 warps 18.6 us, 8 warps 18.0, 16 warps 17.3;
-// plain 15.6, 15.0, 15.0).
-using Cfg16 = gb300::KernelConfig<128, 256, 3, 16>;
+// The same 128 x 256 tiles with sixteen epilogue warps (four per TMEM lane quarter, 64
+// columns each, 96 registers): the whole-tile kernel when all tiles fit one wave, where every
+// CTA's epilogue is an exposed tail that more warps shorten (2048^3 + bias + GELU, same box: 4
+// warps 18.6 us, 8 warps 18.0, 16 warps 17.3; plain 15.6, 15.0, 15.0). Each CTA has one tile,
+// so its output staging overlays the idle operand ring, which leaves room for a fourth stage
+// (2048^3 14.7 -> 13.9 us, 2048 x 2048 x 8192 55.5 -> 46.1, 1024 x 4096 x 4096 + bias + GELU
+// 27.5 -> 24.8); two 128-wide stages in the same space were 3-9 % slower than three 64-wide.
+using Cfg16 = gb300::KernelConfig<128, 256, 4, 16, 64, true>;
 // The softmax epilogue's kernel: 128 x 256 tiles, 3-stage ring, sixteen epilogue warps.
 using SoftCfg = gb300::SoftmaxConfig<3>;
-// Split-K runs on the eight-warp instance: twice the warps to stage the partial and to
-// read the other CTAs' partials over DSMEM (measured 2-5 % faster than four on 5 of 6
-// few-tile shapes); its 3-stage ring (144 KB) holds the 128 KB partial.
-using SplitCfg = Cfg8;
+// Split-K runs on an instance with eight epilogue warps (two per TMEM lane quarter, each with
+// half of the columns): twice the warps to stage the partial and to read the other CTAs'
+// partials over DSMEM (measured 2-5 % faster than four on 5 of 6 few-tile shapes). Its
+// epilogue writes C with plain stores, so the (unused) output staging overlays the ring, and
+// the ring has four stages (192 KB; it holds the 128 KB partial): 256 x 4096 x 8192 23.2 ->
+// 21.3 us, 2048 x 1024 x 8192 + bias + GELU 34.4 -> 32.3 against three.
+using SplitCfg = gb300::KernelConfig<128, 256, 4, 8, 64, true>;
 #ifndef GB300_GROUP_PANEL_MB
 #define GB300_GROUP_PANEL_MB 32
 #endif
@@ -279,9 +282,9 @@ const char *plan_kernel_name(PlanKind k)
     switch (k) {
     case PLAN_PAIR: return "gemm_tcgen05_pair_kernel<PairConfig<256,3,4,128>>";
     case PLAN_TILES: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_TILES>";
-    case PLAN_TILES16: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,16>,SCHED_TILES>";
+    case PLAN_TILES16: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,16,64,true>,SCHED_TILES>";
     case PLAN_STREAMK: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_STREAM_K>";
-    case PLAN_SPLITK: return "gemm_tcgen05_kernel<KernelConfig<128,256,3,8>,SCHED_SPLIT_K>";
+    case PLAN_SPLITK: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,8,64,true>,SCHED_SPLIT_K>";
     case PLAN_ROWCLUSTER: return "gemm_softmax_kernel<SoftmaxConfig<3>,false>";
     case PLAN_ROWCLUSTER2: return "gemm_softmax_kernel<SoftmaxConfig<3>,true>";
     }
@@ -410,7 +413,10 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     const Plan pl = make_plan(ctx, M, N, K, epilogue);
     // K per ring stage of the chosen kernel: A goes in 64-wide boxes either way, B in boxes
     // of that many rows
-    const int bk = pl.kind == PLAN_PAIR ? PairCfg::BK : Cfg::BK;
+    const int bk = pl.kind == PLAN_PAIR ? PairCfg::BK : pl.kind == PLAN_TILES16 ? Cfg16::BK : Cfg::BK;
+    // Cfg16 stages its output in the operand ring: one tile per CTA at most
+    if (pl.kind == PLAN_TILES16 && pl.grid < pl.num_tiles)
+        return GEMM_ERR_ARG;
     if (K > 0) {
         if (!encode_2d(ctx, &ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), Cfg::BK, Cfg::BM) ||
             !encode_2d(ctx, &tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), Cfg::B_BOX_N,

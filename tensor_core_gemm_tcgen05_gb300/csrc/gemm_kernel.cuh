@@ -93,13 +93,20 @@ struct GemmParams {
     int64_t ldc = 0;                 // row stride of C in elements (split-K writes C directly)
 };
 
-template <int BM_, int BN_, int STAGES_, int EPI_WARPS_ = 4>
+// BK_: K per stage, 64 or 128 (one or two 128-byte swizzle atoms of A; every stage ends in one
+// tcgen05.commit, so longer stages commit half as often). STORE_IN_RING_: the output staging
+// boxes overlay the operand ring instead of having their own space; only for launches that
+// give each CTA at most one tile (the ring is idle once its accumulator is complete).
+template <int BM_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int BK_ = 64, bool STORE_IN_RING_ = false>
 struct KernelConfig {
     static constexpr int BM = BM_;          // rows of A / C per tile (= UMMA M, = TMEM lanes)
     static constexpr int BN = BN_;          // columns of B / C per tile (= UMMA N)
-    static constexpr int BK = 64;           // K per stage: 64 FP16 = one 128-byte swizzle row
+    static constexpr int BK = BK_;          // K per stage
     static constexpr int UMMA_K = 16;       // K per tcgen05.mma of kind::f16
     static constexpr int STAGES = STAGES_;
+    static constexpr bool STORE_IN_RING = STORE_IN_RING_;
+    static constexpr int A_ATOM_BYTES = BM * 64 * 2;   // 64 K-columns of A: one swizzle atom wide
+    static constexpr int A_ATOMS = BK / 64;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BOX_N = 64;                 // N per TMA box of B (128 bytes)
     static constexpr int B_BOXES = BN / B_BOX_N;
@@ -120,9 +127,12 @@ struct KernelConfig {
     // after the ring: barriers, TMEM address, stop flag; then one BN-wide bias slice per
     // epilogue warp (FP16)
     static constexpr int BIAS_OFFSET = STAGES * STAGE_BYTES + ((NUM_BARS * 8 + 16 + 15) / 16) * 16;
-    // then, 1024-aligned, two 32 x 32 FP16 output staging boxes per epilogue warp
-    static constexpr int STORE_OFFSET = ((BIAS_OFFSET + NUM_EPI_WARPS * BN * 2 + 1023) / 1024) * 1024;
-    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES;
+    // then, 1024-aligned, two 32 x 32 FP16 output staging boxes per epilogue warp (or, with
+    // STORE_IN_RING, the same boxes at the start of the operand ring)
+    static constexpr int BIAS_END = BIAS_OFFSET + NUM_EPI_WARPS * BN * 2;
+    static constexpr int STORE_OFFSET = STORE_IN_RING ? 0 : ((BIAS_END + 1023) / 1024) * 1024;
+    static constexpr int SMEM_BYTES =
+        1024 /* alignment slack */ + (STORE_IN_RING ? BIAS_END : STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES);
 
     static_assert(BM == 128, "one CTA, M = 128: TMEM lane i holds tile row i");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
@@ -132,6 +142,9 @@ struct KernelConfig {
     static_assert((BN / 32) % EPI_COL_GROUPS == 0, "column chunks split evenly between warps");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
     static_assert(NUM_EPI_WARPS * PART_WARP_BYTES <= STAGES * STAGE_BYTES, "partials fit the operand ring");
+    static_assert(BK == 64 || BK == 128, "one or two swizzle atoms of K per stage");
+    static_assert(!STORE_IN_RING || NUM_EPI_WARPS * EPI_STORE_WARP_BYTES <= STAGES * STAGE_BYTES,
+                  "output staging fits the operand ring");
 };
 
 // UMMA shared-memory descriptor for a 128-byte-swizzled operand tile.
@@ -808,7 +821,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     } else {
                         const uint32_t fb = full0 + 8u * stage;
                         mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-                        tma_load_2d(sA + stage * Cfg::A_BYTES, &tmap_a, fb, kb * BK, mb * BM);
+#pragma unroll
+                        for (int a = 0; a < Cfg::A_ATOMS; ++a)
+                            tma_load_2d(sA + stage * Cfg::A_BYTES + a * Cfg::A_ATOM_BYTES, &tmap_a, fb,
+                                        kb * BK + 64 * a, mb * BM);
 #pragma unroll
                         for (int j = 0; j < Cfg::B_BOXES; ++j)
                             tma_load_2d(sB + stage * Cfg::B_BYTES + j * Cfg::B_BOX_BYTES, &tmap_b, fb,
@@ -835,9 +851,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             // Shared-memory descriptors of stage 0's A and B; every other step is a constant
             // offset in the start-address field (16-byte units; addresses stay below 256 KB, so
             // the 14-bit field never carries). A, K-major: the next 16 K-values are 32 bytes
-            // further along each 128-byte swizzled row, 8-row groups 1024 bytes apart. B,
-            // MN-major: 16 K-rows are 2048 bytes further, 8-row K groups 1024 bytes apart (SBO),
-            // 64-column N atoms one box apart (LBO).
+            // further along each 128-byte swizzled row, 8-row groups 1024 bytes apart, the
+            // second 64 K-values (BK = 128) one atom further. B, MN-major: 16 K-rows are 2048
+            // bytes further, 8-row K groups 1024 bytes apart (SBO), 64-column N atoms one box
+            // apart (LBO).
             const uint64_t a_desc0 = sw128_desc(sA, 16, 1024), b_desc0 = sw128_desc(sB, Cfg::B_BOX_BYTES, 1024);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
@@ -861,8 +878,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     const uint64_t b_st = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
 #pragma unroll
                     for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk)
-                        umma_f16<1>(d_tmem, a_st + static_cast<uint64_t>(2 * kk), b_st + static_cast<uint64_t>(128 * kk), IDESC,
-                                    (kb != k0 || kk != 0) ? 1u : 0u);
+                        umma_f16<1>(d_tmem,
+                                    a_st + static_cast<uint64_t>((kk >> 2) * (Cfg::A_ATOM_BYTES >> 4) + 2 * (kk & 3)),
+                                    b_st + static_cast<uint64_t>(128 * kk), IDESC, (kb != k0 || kk != 0) ? 1u : 0u);
                     umma_commit(empty0 + 8u * stage);   // slot free once these MMAs have read it
                     if (++stage == STAGES) {
                         stage = 0;
