@@ -38,7 +38,11 @@ using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS, GB300
 // so its output staging overlays the idle operand ring, which leaves room for a fourth stage
 // (2048^3 14.7 -> 13.9 us, 2048 x 2048 x 8192 55.5 -> 46.1, 1024 x 4096 x 4096 + bias + GELU
 // 27.5 -> 24.8); two 128-wide stages in the same space were 3-9 % slower than three 64-wide.
-using Cfg16 = gb300::KernelConfig<128, 256, 4, 16, 64, true>;
+// The last four k-blocks go into the left half of the accumulator first (HALF_TAIL), so that
+// half's epilogue warps start during the right half's MMAs: 0.1-4 % on one-wave shapes (the
+// right half's N = 128 MMAs use the whole shared-memory bandwidth, which the overlapped
+// epilogue's staging also needs; giving every warp a chunk of each half was no better).
+using Cfg16 = gb300::KernelConfig<128, 256, 4, 16, 64, true, true>;
 // The softmax epilogue's kernel: 128 x 256 tiles, 3-stage ring, sixteen epilogue warps.
 using SoftCfg = gb300::SoftmaxConfig<3>;
 // Split-K runs on an instance with eight epilogue warps (two per TMEM lane quarter, each with
@@ -282,7 +286,7 @@ const char *plan_kernel_name(PlanKind k)
     switch (k) {
     case PLAN_PAIR: return "gemm_tcgen05_pair_kernel<PairConfig<256,3,4,128>>";
     case PLAN_TILES: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_TILES>";
-    case PLAN_TILES16: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,16,64,true>,SCHED_TILES>";
+    case PLAN_TILES16: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,16,64,true,true>,SCHED_TILES>";
     case PLAN_STREAMK: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_STREAM_K>";
     case PLAN_SPLITK: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,8,64,true>,SCHED_SPLIT_K>";
     case PLAN_ROWCLUSTER: return "gemm_softmax_kernel<SoftmaxConfig<3>,false>";

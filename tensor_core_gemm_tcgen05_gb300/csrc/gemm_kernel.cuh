@@ -97,7 +97,11 @@ struct GemmParams {
 // tcgen05.commit, so longer stages commit half as often). STORE_IN_RING_: the output staging
 // boxes overlay the operand ring instead of having their own space; only for launches that
 // give each CTA at most one tile (the ring is idle once its accumulator is complete).
-template <int BM_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int BK_ = 64, bool STORE_IN_RING_ = false>
+// HALF_TAIL_ (with STORE_IN_RING_, whole tiles): the last STAGES k-blocks of a tile are
+// multiplied into the left half of the accumulator (N = BN / 2) first, then into the right
+// half, so that the epilogue warps of the left columns start while the right half's MMAs run.
+template <int BM_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int BK_ = 64, bool STORE_IN_RING_ = false,
+          bool HALF_TAIL_ = false>
 struct KernelConfig {
     static constexpr int BM = BM_;          // rows of A / C per tile (= UMMA M, = TMEM lanes)
     static constexpr int BN = BN_;          // columns of B / C per tile (= UMMA N)
@@ -105,6 +109,7 @@ struct KernelConfig {
     static constexpr int UMMA_K = 16;       // K per tcgen05.mma of kind::f16
     static constexpr int STAGES = STAGES_;
     static constexpr bool STORE_IN_RING = STORE_IN_RING_;
+    static constexpr bool HALF_TAIL = HALF_TAIL_;
     static constexpr int A_ATOM_BYTES = BM * 64 * 2;   // 64 K-columns of A: one swizzle atom wide
     static constexpr int A_ATOMS = BK / 64;
     static constexpr int A_BYTES = BM * BK * 2;
@@ -119,8 +124,14 @@ struct KernelConfig {
     static constexpr int EPI_COL_GROUPS = NUM_EPI_WARPS / 4;   // warps sharing a TMEM quarter
     static constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
     // full[s], empty[s], acc_full[b], acc_empty[b], drain, one stream-K partial barrier per
-    // epilogue warp
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + NUM_EPI_WARPS;
+    // epilogue warp, left_half (HALF_TAIL: the left half of the accumulator is complete)
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + NUM_EPI_WARPS + 1;
+    // HALF_TAIL: output staging of the epilogue warps of the left columns, in the left halves
+    // of the stages' B operands (no MMA reads those once the left half is complete); the
+    // other warps stage where STORE_IN_RING puts them, at the start of the ring (A), used
+    // only after every MMA is complete
+    static constexpr int LEFT_WARPS = NUM_EPI_WARPS / 2;
+    static constexpr int LEFT_STAGE_WARPS = (BK * BN) / EPI_STORE_WARP_BYTES;   // B_BYTES / 2 per stage
     // stream-K: one epilogue warp's share of a partial accumulator (32 rows x its columns,
     // FP32), as stored in the workspace and as pulled into the operand ring
     static constexpr int PART_WARP_BYTES = (BN / EPI_COL_GROUPS) * 32 * 4;
@@ -145,6 +156,10 @@ struct KernelConfig {
     static_assert(BK == 64 || BK == 128, "one or two swizzle atoms of K per stage");
     static_assert(!STORE_IN_RING || NUM_EPI_WARPS * EPI_STORE_WARP_BYTES <= STAGES * STAGE_BYTES,
                   "output staging fits the operand ring");
+    static_assert(!HALF_TAIL || (STORE_IN_RING && EPI_COL_GROUPS % 2 == 0 && (BK * BN) % EPI_STORE_WARP_BYTES == 0 &&
+                                 LEFT_WARPS <= STAGES * LEFT_STAGE_WARPS &&
+                                 NUM_EPI_WARPS * EPI_STORE_WARP_BYTES <= STAGES * A_BYTES),
+                  "half-tail split: whole column groups per half, staging in the left B halves and in A");
 };
 
 // UMMA shared-memory descriptor for a 128-byte-swizzled operand tile.
@@ -746,6 +761,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr uint32_t IDESC = idesc_f16_f32<BM, BN>();
+    constexpr uint32_t IDESC_HALF = idesc_f16_f32<BM, BN / 2>();
+    static_assert(!Cfg::HALF_TAIL || SCHED == SCHED_TILES, "the half tail is for whole-tile epilogues");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -760,6 +777,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const uint32_t full0 = bar0, empty0 = bar0 + 8u * STAGES;
     const uint32_t accf0 = bar0 + 16u * STAGES, acce0 = accf0 + 8u * Cfg::ACC_BUFS;
     const uint32_t drain = acce0 + 8u * Cfg::ACC_BUFS, part0 = drain + 8u;
+    const uint32_t left_half = part0 + 8u * Cfg::NUM_EPI_WARPS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     uint4 *bias_stage = reinterpret_cast<uint4 *>(sp + Cfg::BIAS_OFFSET);
@@ -780,6 +798,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         mbar_init(drain, 1);
         for (int w = 0; w < Cfg::NUM_EPI_WARPS; ++w)
             mbar_init(part0 + 8u * w, 1);
+        mbar_init(left_half, 1);
         *abort_flag = 0;
         fence_mbar_init();
         if (p.num_kb > 0) {
@@ -868,6 +887,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                // k-blocks [tail, k1) go into the left half only, and stay in the ring for the
+                // right half below (HALF_TAIL; otherwise tail = k1)
+                const int tail = Cfg::HALF_TAIL ? max(k0, k1 - STAGES) : k1;
+                int tail_stage = stage;
                 for (int kb = k0; kb < k1; ++kb) {
                     if (!wait_bounded(full0 + 8u * stage, phase, wc, ERR_MMA_OPERANDS)) {
                         ok = false;
@@ -876,12 +899,22 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     tc_fence_after_sync();
                     const uint64_t a_st = a_desc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
                     const uint64_t b_st = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
+                    if (Cfg::HALF_TAIL && kb >= tail) {
+                        if (kb == tail)
+                            tail_stage = stage;
 #pragma unroll
-                    for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk)
-                        umma_f16<1>(d_tmem,
-                                    a_st + static_cast<uint64_t>((kk >> 2) * (Cfg::A_ATOM_BYTES >> 4) + 2 * (kk & 3)),
-                                    b_st + static_cast<uint64_t>(128 * kk), IDESC, (kb != k0 || kk != 0) ? 1u : 0u);
-                    umma_commit(empty0 + 8u * stage);   // slot free once these MMAs have read it
+                        for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk)
+                            umma_f16<1>(d_tmem,
+                                        a_st + static_cast<uint64_t>((kk >> 2) * (Cfg::A_ATOM_BYTES >> 4) + 2 * (kk & 3)),
+                                        b_st + static_cast<uint64_t>(128 * kk), IDESC_HALF, (kb != k0 || kk != 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk)
+                            umma_f16<1>(d_tmem,
+                                        a_st + static_cast<uint64_t>((kk >> 2) * (Cfg::A_ATOM_BYTES >> 4) + 2 * (kk & 3)),
+                                        b_st + static_cast<uint64_t>(128 * kk), IDESC, (kb != k0 || kk != 0) ? 1u : 0u);
+                        umma_commit(empty0 + 8u * stage);   // slot free once these MMAs have read it
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -889,6 +922,24 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 }
                 if (!ok)
                     break;
+                if constexpr (Cfg::HALF_TAIL) {
+                    umma_commit(left_half);   // columns [0, BN / 2) complete (also when K = 0)
+                    // the right half of the tail k-blocks: B from its second half of N atoms. The
+                    // tail's slots are not released: each CTA has one tile, no load waits for them.
+                    int st = tail_stage;
+                    for (int kb = tail; kb < k1; ++kb) {
+                        const uint64_t a_st = a_desc0 + static_cast<uint64_t>(st * (Cfg::A_BYTES >> 4));
+                        const uint64_t b_st =
+                            b_desc0 + static_cast<uint64_t>(st * (Cfg::B_BYTES >> 4) + ((Cfg::B_BYTES / 2) >> 4));
+#pragma unroll
+                        for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk)
+                            umma_f16<1>(d_tmem + static_cast<uint32_t>(BN / 2),
+                                        a_st + static_cast<uint64_t>((kk >> 2) * (Cfg::A_ATOM_BYTES >> 4) + 2 * (kk & 3)),
+                                        b_st + static_cast<uint64_t>(128 * kk), IDESC_HALF, (kb != k0 || kk != 0) ? 1u : 0u);
+                        if (++st == STAGES)
+                            st = 0;
+                    }
+                }
                 umma_commit(accf0 + 8u * acc);          // accumulator complete
                 if (++acc == Cfg::ACC_BUFS) {
                     acc = 0;
@@ -908,10 +959,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         constexpr int CHUNKS = BN / 32 / Cfg::EPI_COL_GROUPS;   // 32-column chunks per warp
         const int c_begin = ((warp - 2) >> 2) * CHUNKS;
         uint4 *my_bias = bias_stage + (warp - 2) * (BN / 8);   // this warp's BN-wide bias slice
-        const uint32_t my_stage = store_stage + static_cast<uint32_t>(warp - 2) * EPI_STORE_WARP_BYTES;
+        // HALF_TAIL: the warps of columns [0, BN / 2) read the accumulator once its left half is
+        // complete and stage their output in the stages' left B halves (4 KB per warp)
+        const bool left = Cfg::HALF_TAIL && c_begin * 32 < BN / 2;
+        const uint32_t my_stage =
+            left ? sB + static_cast<uint32_t>(((warp - 2) / Cfg::LEFT_STAGE_WARPS) * Cfg::B_BYTES +
+                                              ((warp - 2) % Cfg::LEFT_STAGE_WARPS) * EPI_STORE_WARP_BYTES)
+                 : store_stage + static_cast<uint32_t>(warp - 2) * EPI_STORE_WARP_BYTES;
         uint32_t box_sel = 0;
         int acc = 0;
-        uint32_t acc_phase = 0;
+        uint32_t acc_phase = 0, left_phase = 0;
         const int ew = warp - 2;   // this warp's stream-K flag and partial-barrier index
         // floats per workspace slot, and the offset of this warp's share in a slot
         constexpr int64_t SLOT = static_cast<int64_t>(BM) * BN;
@@ -940,7 +997,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 const uint4 bv = bias_fetch(p, nb * BN, lane);
                 // all lanes poll (see wait_warp): fewer issue slots taken from the producer and
                 // MMA threads than one lane spinning (2048^3 at the power limit: 19.4 -> 18.6 us)
-                int ok = wait_warp(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR, lane) ? 1 : 0;
+                int ok = wait_warp(left ? left_half : accf0 + 8u * acc, left ? left_phase : acc_phase, wc,
+                                   ERR_EPILOGUE_ACCUMULATOR, lane) ? 1 : 0;
+                left_phase ^= 1u;
                 if (!ok)
                     break;
                 tc_fence_after_sync();

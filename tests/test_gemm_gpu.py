@@ -104,6 +104,27 @@ def test_single_tile_identity(kctx):
     assert torch.equal(C2, A2)
 
 
+@pytest.mark.parametrize("K", [64, 192, 256, 320, 512])
+def test_split_tail_identity(kctx, K):
+    # When every tile has its own CTA, the last k-blocks (up to four) are multiplied into the
+    # left 128 columns of the accumulator first and into the right 128 afterwards. With B = I
+    # (K x 256, ones on the diagonal) C is A's first 256 columns exactly, whichever half and
+    # whichever k-block (full-width or split) each column's ones fall in.
+    A = inputs.random_fp16((256, K), 11 + K)
+    B = torch.eye(K, 256, dtype=torch.float16)
+    C = run_guarded(kctx, A, B, None, g.EPI_NONE)
+    want = torch.zeros(256, 256, dtype=torch.float16)
+    want[:, :min(K, 256)] = A[:, :256]
+    assert torch.equal(C, want)
+
+
+@pytest.mark.parametrize("shape", [(256, 136, 200), (130, 392, 256), (128, 256, 192), (200, 520, 4160)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_split_tail_epilogues(kctx, shape):
+    # right halves partly or wholly past N, fewer k-blocks than the tail, a ragged last k-block
+    check(kctx, *shape, epi=g.EPI_GELU, with_bias=True, seed=shape[2])
+
+
 def test_all_ones_gives_k(kctx):
     ctx = kctx
     for K in (64, 2048):
