@@ -158,7 +158,9 @@ int gemm_num_sms(gemm_ctx *ctx);
  * the context's current debug flags: writes a NUL-terminated description of at most len - 1
  * characters to `buf` (host memory owned by the caller), of the form
  *   "<kernel instance> grid=<CTAs> cluster=<CTAs per cluster> tiles=<output tiles>",
- * e.g. "gemm_tcgen05_pair_kernel<PairConfig<256,6,4>> grid=148 cluster=2 tiles=2112".
+ * e.g. "gemm_tcgen05_pair_kernel<PairConfig<256,3,4,128>> grid=152 cluster=2 tiles=2112",
+ * followed by " (last <n> split in N-halves)" when the pair kernel runs its last n tiles as
+ * two half-width work units each.
  * The kernel instance names the template instance as it appears in a profiler's kernel
  * list. Launches nothing and touches no device memory. Returns GEMM_OK, or the status
  * gemm_run would return for these sizes and epilogue (GEMM_ERR_ARG, GEMM_ERR_ALIGN), or

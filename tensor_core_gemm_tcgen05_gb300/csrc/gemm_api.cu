@@ -279,6 +279,7 @@ struct Plan {
     int m_blocks = 0, n_blocks = 0, num_tiles = 0, group_m = 1;
     int split = 0, row_cluster = 0, smx_span = 0, smx_two_pass = 0;
     int64_t sk_units = 0;
+    int pair_split_from = 0, pair_units = 0;   // pair kernel: tiles kept whole, work units
 };
 
 const char *plan_kernel_name(PlanKind k)
@@ -356,6 +357,13 @@ Plan make_plan(const gemm_ctx *ctx, int M, int N, int K, int epilogue)
         pl.group_m = raster_group(pl.m_blocks, PairCfg::BM, K);
         pl.cluster = 2;
         pl.grid = 2 * std::min(pl.num_tiles, ctx->max_clusters);
+        // A last round of tiles that at most half of the pairs would work on (8192^3: 1024
+        // tiles on 76 pairs leave 36) runs as twice as many N-halves, one per pair: that
+        // round takes half as long.
+        const int pairs = pl.grid / 2;
+        const int last = pl.num_tiles % pairs;
+        pl.pair_split_from = (last > 0 && 2 * last <= pairs) ? pl.num_tiles - last : pl.num_tiles;
+        pl.pair_units = pl.pair_split_from + 2 * (pl.num_tiles - pl.pair_split_from);
         return pl;
     }
     pl.m_blocks = (M + Cfg::BM - 1) / Cfg::BM;
@@ -453,6 +461,8 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     p.row_cluster = pl.row_cluster;
     p.smx_span = pl.smx_span;
     p.smx_two_pass = pl.smx_two_pass;
+    p.pair_split_from = pl.pair_split_from;
+    p.pair_units = pl.pair_units;
     if (pl.kind == PLAN_STREAMK) {
         p.sk_units = pl.sk_units;
         p.sk_ws = ctx->sk_ws;
@@ -921,8 +931,11 @@ int gemm_describe(gemm_ctx *ctx, int64_t M, int64_t N, int64_t K, int epilogue, 
         return GEMM_OK;
     }
     const Plan pl = make_plan(ctx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), epilogue);
-    std::snprintf(buf, static_cast<size_t>(len), "%s grid=%d cluster=%d tiles=%d", plan_kernel_name(pl.kind),
-                  pl.grid, pl.cluster, pl.num_tiles);
+    const int n = std::snprintf(buf, static_cast<size_t>(len), "%s grid=%d cluster=%d tiles=%d",
+                                plan_kernel_name(pl.kind), pl.grid, pl.cluster, pl.num_tiles);
+    if (pl.kind == PLAN_PAIR && pl.pair_units > pl.num_tiles && n > 0 && n < len)
+        std::snprintf(buf + n, static_cast<size_t>(len - n), " (last %d split in N-halves)",
+                      pl.num_tiles - pl.pair_split_from);
     return GEMM_OK;
 }
 

@@ -91,6 +91,10 @@ struct GemmParams {
     int smx_two_pass = 0;            // softmax kernel: 1 = statistics pass, then output pass
     int split = 0;                   // split-K: CTAs per cluster, each with 1/split of the k-blocks
     int64_t ldc = 0;                 // row stride of C in elements (split-K writes C directly)
+    // pair kernel: tiles [0, pair_split_from) are whole work units; each later tile is two
+    // units, its left and right N-halves; pair_units = the number of units
+    int pair_split_from = 0;
+    int pair_units = 0;
 };
 
 // BK_: K per stage, 64 or 128 (one or two 128-byte swizzle atoms of A; every stage ends in one
@@ -581,9 +585,10 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *flag, const WaitCtl &w
 template <int CHUNKS>
 __device__ __forceinline__ void epilogue_tile(const GemmParams &p, uint32_t taddr, int n_first, int row0,
                                               const uint4 *sbias, const CUtensorMap *tmap_c, uint32_t stage,
-                                              uint32_t &box_sel, int lane)
+                                              uint32_t &box_sel, int lane, int n_end = 0x7fffffff)
 {
-    const int valid = min(CHUNKS, (p.N - n_first + 31) / 32);
+    // columns [n_first, min(N, n_end)) of this warp's rows, 32 per chunk
+    const int valid = min(CHUNKS, (min(p.N, n_end) - n_first + 31) / 32);
     if (valid <= 0 || row0 >= p.M)
         return;   // nothing of this warp's part of the tile is inside C
     const bool has_acc = p.num_kb > 0;   // K = 0: the empty sum, no accumulator to read

@@ -17,6 +17,11 @@
 //    kernel (epilogue_tile), overlapping the next tile's MMAs (two accumulators).
 // Waits are bounded as in the one-CTA kernel; a CTA that gives up also raises the stop
 // flag of its peer, and both CTAs meet at a cluster barrier before Tensor Memory is freed.
+//
+// Work units: pair p takes units p, p + P, p + 2P, ... (P pairs). When the tiles leave a last
+// round that at most half of the pairs would work on, the host splits each tile of that round
+// into its left and right N-halves (256 x BN/2, UMMA N = BN/2, one B box per CTA), so that
+// the round takes half as long and no reduction is needed.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -60,6 +65,19 @@ struct PairConfig {
     static_assert((BN / 32) % EPI_COL_GROUPS == 0, "column chunks split evenly between warps");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 };
+
+// Work unit u: its tile t and which part of it (0: whole, 1: left half, 2: right half).
+__device__ __forceinline__ void pair_unit(const GemmParams &p, int u, int &t, int &half)
+{
+    const int f = p.pair_split_from;
+    if (u < f) {
+        t = u;
+        half = 0;
+    } else {
+        t = f + ((u - f) >> 1);
+        half = 1 + ((u - f) & 1);
+    }
+}
 
 __device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v)
 {
@@ -126,6 +144,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
 {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr uint32_t IDESC = idesc_f16_f32<BM, BN>();
+    constexpr uint32_t IDESC_HALF = idesc_f16_f32<BM, BN / 2>();
+    static_assert(Cfg::B_BOXES % 2 == 0, "a half tile takes half of each CTA's B boxes");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -149,6 +169,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
     const bool leader = rank == 0;
     const int cluster_id = static_cast<int>(blockIdx.x >> 1);
     const int num_clusters = static_cast<int>(gridDim.x >> 1);
+    const int num_units = p.pair_units;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -193,9 +214,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_parity = 0;
             bool ok = true, withhold = leader && (p.debug & DEBUG_WITHHOLD_FIRST_LOAD) != 0;
-            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-                int mb, nb;
+            for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
+                int t, half, mb, nb;
+                pair_unit(p, u, t, half);
                 tile_coords(p, t, mb, nb);
+                // this CTA's B columns: its BN/2 of a whole tile, its BN/4 of a half
+                const int b_boxes = half ? Cfg::B_BOXES / 2 : Cfg::B_BOXES;
+                const int b_col0 = nb * BN + (half == 2 ? BN / 2 : 0) + static_cast<int>(rank) * b_boxes * Cfg::B_BOX_N;
+                const uint32_t tx = 2u * static_cast<uint32_t>(Cfg::A_BYTES + b_boxes * Cfg::B_BOX_BYTES);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!pair_wait(empty0 + 8u * stage, phase ^ 1u, wc, ERR_PRODUCER_SLOT)) {
                         ok = false;
@@ -206,16 +232,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
                     } else {
                         const uint32_t fb = full0_leader + 8u * stage;
                         if (leader)   // CTA 0's barrier counts the bytes of both CTAs
-                            mbar_arrive_expect_tx(full0 + 8u * stage, 2 * Cfg::STAGE_BYTES);
+                            mbar_arrive_expect_tx(full0 + 8u * stage, tx);
 #pragma unroll
                         for (int a = 0; a < Cfg::A_ATOMS; ++a)
                             tma_load_2d_pair(sA + stage * Cfg::A_BYTES + a * Cfg::A_ATOM_BYTES, &tmap_a, fb,
                                              kb * BK + 64 * a, mb * BM + static_cast<int>(rank) * Cfg::CTA_BM);
-#pragma unroll
-                        for (int j = 0; j < Cfg::B_BOXES; ++j)
+                        for (int j = 0; j < b_boxes; ++j)
                             tma_load_2d_pair(sB + stage * Cfg::B_BYTES + j * Cfg::B_BOX_BYTES, &tmap_b, fb,
-                                             nb * BN + static_cast<int>(rank) * Cfg::CTA_BN + j * Cfg::B_BOX_N,
-                                             kb * BK);
+                                             b_col0 + j * Cfg::B_BOX_N, kb * BK);
                         issued |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     }
@@ -248,7 +272,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+            for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
+                int t, half;
+                pair_unit(p, u, t, half);
+                const uint32_t idesc = half ? IDESC_HALF : IDESC;   // N = BN/2: one B box per CTA
                 if (!pair_wait(acce0 + 8u * acc, acc_phase ^ 1u, wc, ERR_MMA_ACCUMULATOR)) {
                     ok = false;
                     break;
@@ -267,7 +294,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
                     for (int kk = 0; kk < BK / Cfg::UMMA_K; ++kk)
                         umma_f16<2>(d_tmem,
                                     a_st + static_cast<uint64_t>((kk >> 2) * (Cfg::A_ATOM_BYTES >> 4) + 2 * (kk & 3)),
-                                    b_st + static_cast<uint64_t>(128 * kk), IDESC, (kb | kk) != 0 ? 1u : 0u);
+                                    b_st + static_cast<uint64_t>(128 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);
                     umma_commit_pair(empty0 + 8u * stage, 0x3);   // both CTAs' slots are free
                     if (++stage == STAGES) {
                         stage = 0;
@@ -299,10 +326,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
         uint32_t box_sel = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
-            int mb, nb;
+        for (int u = cluster_id; u < num_units; u += num_clusters) {
+            int t, half, mb, nb;
+            pair_unit(p, u, t, half);
             tile_coords(p, t, mb, nb);
-            const uint4 bv = bias_fetch(p, nb * BN, lane);
+            // the unit's first column and width (a half tile's accumulator is columns [0, BN/2))
+            const int n0 = nb * BN + (half == 2 ? BN / 2 : 0);
+            const int n_end = n0 + (half ? BN / 2 : BN);
+            const uint4 bv = bias_fetch(p, n0, lane);
             if (!pair_wait_warp(accf0 + 8u * acc, acc_phase, wc, ERR_EPILOGUE_ACCUMULATOR, lane))
                 break;
             tc_fence_after_sync();
@@ -311,9 +342,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::NUM_THREADS, 1)
                 __syncwarp();
             }
             epilogue_tile<CHUNKS>(p, tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c_begin * 32),
-                                  nb * BN + c_begin * 32, mb * BM + static_cast<int>(rank) * Cfg::CTA_BM + quarter * 32,
+                                  n0 + c_begin * 32, mb * BM + static_cast<int>(rank) * Cfg::CTA_BM + quarter * 32,
                                   p.bias != nullptr ? my_bias + c_begin * 4 : nullptr, &tmap_c, my_stage, box_sel,
-                                  lane);
+                                  lane, n_end);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)

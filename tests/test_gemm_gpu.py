@@ -522,6 +522,35 @@ def test_splitk_cluster_sizes_and_tails(ctx, shape):
         g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
 
 
+@pytest.mark.parametrize("epi,with_bias", [(g.EPI_NONE, False), (g.EPI_GELU, True)])
+def test_pair_last_round_in_n_halves(ctx, epi, with_bias):
+    """Pair kernel with a few more 256 x 256 tiles than pairs: the last round's tiles run as
+    N-halves (256 x 128, one B box per CTA), one per pair. Ragged M, N and K put rows and
+    columns past C in the split tiles; every row is checked against the oracle, and two runs
+    agree bit for bit."""
+    pairs = g.gemm_num_pairs(ctx)
+    if pairs < 4:
+        pytest.skip("the pair kernel cannot run on this device")
+    n_blocks = 4
+    m_blocks = (pairs + 4 + n_blocks - 1) // n_blocks   # pairs + 1 .. pairs + 7 tiles
+    M, N, K = 256 * m_blocks - 100, 256 * n_blocks - 56, 520
+    tiles = m_blocks * n_blocks
+    assert 0 < tiles % pairs <= pairs // 2
+    desc = g.gemm_describe(ctx, M, N, K, epi)
+    assert "pair_kernel" in desc and f"(last {tiles % pairs} split in N-halves)" in desc, desc
+    check(ctx, M, N, K, epi=epi, with_bias=with_bias, seed=77 + epi)
+    dev = torch.device("cuda:0")
+    A = inputs.random_fp16((M, K), 78).to(dev)
+    B = inputs.random_fp16((K, N), 79).to(dev)
+    C1 = torch.empty(M, N, dtype=torch.float16, device=dev)
+    C2 = torch.empty(M, N, dtype=torch.float16, device=dev)
+    g.gemm(ctx, A, B, None, epi, out=C1)
+    g.gemm(ctx, A, B, None, epi, out=C2)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+    assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+
+
 def test_splitk_in_host_column_bands(ctx):
     """Split-K inside gemm_run_host's column bands: each band's C is a slice of a wider
     matrix (row stride N, not the band's width), which split-K writes directly."""
