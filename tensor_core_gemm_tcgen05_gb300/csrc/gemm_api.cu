@@ -67,6 +67,25 @@ int raster_group(int m_blocks, int rows_per_block, int K)
     const int64_t g = kGroupPanelBytes / panel;
     return static_cast<int>(std::max<int64_t>(kMinGroup, std::min<int64_t>(m_blocks, g)));
 }
+
+#ifndef GB300_BALANCED_GROUPS
+#define GB300_BALANCED_GROUPS 1
+#endif
+// Raster groups of about equal size: the group count is m_blocks / target rounded to the
+// nearest integer (at least one), the row-blocks spread evenly (the first `big` groups one
+// larger). A last group of a few row-blocks would stream all of B again for them (M = 8200
+// with 256-row blocks and 16-block groups: 16 + 16 + 1; here 17 + 16).
+void raster_groups(int m_blocks, int rows_per_block, int K, int &group_m, int &big)
+{
+    const int g = raster_group(m_blocks, rows_per_block, K);
+    big = 0;
+    group_m = g;
+    if (!GB300_BALANCED_GROUPS || m_blocks <= 0)
+        return;
+    const int count = std::max(1, (2 * m_blocks + g) / (2 * g));
+    group_m = m_blocks / count;
+    big = m_blocks % count;
+}
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int64_t kSoftmaxMaxCtas = int64_t(1) << 20;   // row softmax grid cap (CTAs loop past it)
 constexpr int kSoftmaxClusterMax = 8;   // softmax: clusters of 1, 2, 4 or 8 CTAs per row block
@@ -276,7 +295,7 @@ struct Plan {
     PlanKind kind = PLAN_TILES;
     int grid = 0;      // CTAs launched
     int cluster = 1;   // CTAs per thread-block cluster (1: no cluster attribute)
-    int m_blocks = 0, n_blocks = 0, num_tiles = 0, group_m = 1;
+    int m_blocks = 0, n_blocks = 0, num_tiles = 0, group_m = 1, group_big = 0;
     int split = 0, row_cluster = 0, smx_span = 0, smx_two_pass = 0;
     int64_t sk_units = 0;
     int pair_split_from = 0, pair_units = 0;   // pair kernel: tiles kept whole, work units
@@ -354,7 +373,7 @@ Plan make_plan(const gemm_ctx *ctx, int M, int N, int K, int epilogue)
         pl.m_blocks = (M + PairCfg::BM - 1) / PairCfg::BM;
         pl.n_blocks = (N + PairCfg::BN - 1) / PairCfg::BN;
         pl.num_tiles = pl.m_blocks * pl.n_blocks;
-        pl.group_m = raster_group(pl.m_blocks, PairCfg::BM, K);
+        raster_groups(pl.m_blocks, PairCfg::BM, K, pl.group_m, pl.group_big);
         pl.cluster = 2;
         pl.grid = 2 * std::min(pl.num_tiles, ctx->max_clusters);
         // A last round of tiles that at most half of the pairs would work on (8192^3: 1024
@@ -369,7 +388,7 @@ Plan make_plan(const gemm_ctx *ctx, int M, int N, int K, int epilogue)
     pl.m_blocks = (M + Cfg::BM - 1) / Cfg::BM;
     pl.n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
     pl.num_tiles = pl.m_blocks * pl.n_blocks;
-    pl.group_m = raster_group(pl.m_blocks, Cfg::BM, K);
+    raster_groups(pl.m_blocks, Cfg::BM, K, pl.group_m, pl.group_big);
     pl.grid = std::min(pl.num_tiles, ctx->num_sms);
     // Split-K when the tiles leave most SMs idle: a cluster of S CTAs per tile, each with
     // 1/S of the k-blocks (at least kSplitKMinBlocks of them), the partials summed over
@@ -457,6 +476,7 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     p.n_blocks = pl.n_blocks;
     p.num_tiles = pl.num_tiles;
     p.group_m = pl.group_m;
+    p.group_big = pl.group_big;
     p.split = pl.split;
     p.row_cluster = pl.row_cluster;
     p.smx_span = pl.smx_span;

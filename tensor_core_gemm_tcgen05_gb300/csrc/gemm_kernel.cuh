@@ -75,6 +75,7 @@ struct GemmParams {
     int M, N, K;
     int m_blocks, n_blocks, num_tiles, num_kb;
     int group_m;           // m-blocks per raster group
+    int group_big = 0;     // the first group_big groups have one m-block more
     int epilogue;          // EPI_*
     const __half *bias;    // N values or nullptr
     __half *C;             // M x N row-major
@@ -191,13 +192,26 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32()
 // Grouped raster: tiles are numbered so that consecutive tile indices (which run at the
 // same time on neighbouring SMs) sweep `group_m` row-blocks of A against successive
 // column-blocks of B, keeping both operand panels hot in L2.
+// The first p.group_big groups have group_m + 1 row-blocks, the rest group_m (the last one
+// possibly fewer when group_big = 0).
 __device__ __forceinline__ void tile_coords(const GemmParams &p, int t, int &mb, int &nb)
 {
-    const int per_group = p.group_m * p.n_blocks;
-    const int g = t / per_group;
-    const int first_m = g * p.group_m;
-    const int rows = min(p.m_blocks - first_m, p.group_m);
-    const int r = t - g * per_group;
+    const int big_rows = p.group_m + 1;
+    const int big_tiles = p.group_big * big_rows * p.n_blocks;
+    int first_m, rows, r;
+    if (t < big_tiles) {
+        const int g = t / (big_rows * p.n_blocks);
+        first_m = g * big_rows;
+        rows = big_rows;
+        r = t - g * big_rows * p.n_blocks;
+    } else {
+        const int u = t - big_tiles;
+        const int per_group = p.group_m * p.n_blocks;
+        const int g = u / per_group;
+        first_m = p.group_big * big_rows + g * p.group_m;
+        rows = min(p.m_blocks - first_m, p.group_m);
+        r = u - g * per_group;
+    }
     mb = first_m + r % rows;
     nb = r / rows;
 }
