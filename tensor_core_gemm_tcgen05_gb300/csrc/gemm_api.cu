@@ -103,6 +103,7 @@ constexpr uint64_t kMinTimeoutNs = 1000000ull;
 // whole tiles, 23 us stream-K).
 constexpr int64_t kStreamKMinUnits = 16;
 constexpr int kSplitKMinBlocks = 8;   // split-K: k-blocks per CTA at least
+constexpr int kPairLongK = 8192;       // pairs for a one-wave problem from this K on
 constexpr int kStreamKMinSpread = 2;
 
 }  // namespace
@@ -362,8 +363,17 @@ Plan make_plan(const gemm_ctx *ctx, int M, int N, int K, int epilogue)
     }
     // 256 x 256 tiles on CTA pairs when there are enough of them to give every pair at
     // least one; otherwise 128 x 256 tiles on single SMs (twice as many tiles to spread).
+    // Also pairs for a long K when at least three quarters of the pairs get a tile and the
+    // single-SM tiles would fit one wave: each pair moves 64 operand bytes per clock of
+    // tensor work from L2 against 96 for a single SM's 128 x 256 tile (more than L2 delivers
+    // to every SM at once), which outweighs the pair's dearer start and 4-warp epilogue
+    // once K >= 8192 (64 pair tiles: 2048 x 2048 x 8192 +1.6 %, x 16384 +7.1 %, 4096 x 1024
+    // x 8192 +5.2 %; at K = 6144 -3.7 %).
     const int pair_tiles = ((M + PairCfg::BM - 1) / PairCfg::BM) * ((N + PairCfg::BN - 1) / PairCfg::BN);
-    bool pair = ctx->max_clusters > 0 && pair_tiles >= ctx->max_clusters;
+    const int one_tiles = ((M + Cfg::BM - 1) / Cfg::BM) * ((N + Cfg::BN - 1) / Cfg::BN);
+    bool pair = ctx->max_clusters > 0 &&
+                (pair_tiles >= ctx->max_clusters || (K >= kPairLongK && 4 * pair_tiles >= 3 * ctx->max_clusters &&
+                                                     one_tiles <= ctx->num_sms));
     if (ctx->debug & (GEMM_DEBUG_FORCE_SINGLE | GEMM_DEBUG_FORCE_SPLITK))
         pair = false;
     if ((ctx->debug & GEMM_DEBUG_FORCE_PAIR) && ctx->max_clusters > 0)

@@ -551,6 +551,30 @@ def test_pair_last_round_in_n_halves(ctx, epi, with_bias):
     assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
 
 
+def test_long_k_one_wave_runs_on_pairs(ctx):
+    """A one-wave problem with K >= 8192 and enough 256 x 256 tiles for three quarters of the
+    pairs runs on the pair kernel (its main loop needs fewer L2 bytes per flop); the same
+    sizes with K = 4096 stay on single SMs. Sampled rows, the last ones included, against the
+    oracle, ragged M, N and K."""
+    pairs = g.gemm_num_pairs(ctx)
+    if pairs < 4:
+        pytest.skip("the pair kernel cannot run on this device")
+    n_blocks = 8
+    m_blocks = max(1, (3 * pairs + 3) // 4 + n_blocks - 1) // n_blocks   # >= 3/4 of the pairs
+    M, N = 256 * m_blocks - 48, 256 * n_blocks - 16
+    if ((M + 127) // 128) * ((N + 255) // 256) > g.gemm_num_sms(ctx) or m_blocks * n_blocks > pairs:
+        pytest.skip("no one-wave shape with that many pair tiles on this device")
+    assert "pair_kernel" in g.gemm_describe(ctx, M, N, 8200, g.EPI_GELU)
+    assert "pair_kernel" not in g.gemm_describe(ctx, M, N, 4096, g.EPI_GELU)
+    K = 8200
+    A = inputs.random_fp16((M, K), 95)
+    B = inputs.random_fp16((K, N), 96)
+    bias = inputs.random_fp16((N,), 97)
+    C = run_guarded(ctx, A, B, bias, g.EPI_GELU)
+    rows = inputs.sample_rows(M, 160, seed=11, include_last=4).numpy()
+    assert_parity(C.numpy()[rows], oracle_ref(A, B, bias, g.EPI_GELU, rows=rows), "long-K pair")
+
+
 def test_splitk_in_host_column_bands(ctx):
     """Split-K inside gemm_run_host's column bands: each band's C is a slice of a wider
     matrix (row stride N, not the band's width), which split-K writes directly."""
