@@ -364,9 +364,9 @@ Plan make_plan(const gemm_ctx *ctx, int M, int N, int K, int epilogue)
     // 256 x 256 tiles on CTA pairs when there are enough of them to give every pair at
     // least one; otherwise 128 x 256 tiles on single SMs (twice as many tiles to spread).
     // Also pairs for a long K when at least three quarters of the pairs get a tile and the
-    // single-SM tiles would fit one wave: each pair moves 64 operand bytes per clock of
-    // tensor work from L2 against 96 for a single SM's 128 x 256 tile (more than L2 delivers
-    // to every SM at once), which outweighs the pair's dearer start and 4-warp epilogue
+    // single-SM tiles would fit one wave: each pair's SM moves 64 operand bytes per clock of
+    // tensor work from L2 against 96 for a single SM's 128 x 256 tile (on 128 SMs about all
+    // that L2 delivers at once), which outweighs the pair's dearer start and 4-warp epilogue
     // once K >= 8192 (64 pair tiles: 2048 x 2048 x 8192 +1.6 %, x 16384 +7.1 %, 4096 x 1024
     // x 8192 +5.2 %; at K = 6144 -3.7 %).
     const int pair_tiles = ((M + PairCfg::BM - 1) / PairCfg::BM) * ((N + PairCfg::BN - 1) / PairCfg::BN);
