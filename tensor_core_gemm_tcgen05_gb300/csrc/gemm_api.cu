@@ -31,6 +31,12 @@ using Cfg = gb300::KernelConfig<128, 256, 4, GB300_EPI_WARPS>;
 #define GB300_PAIR_BK 128
 #endif
 using PairCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, GB300_EPI_WARPS, GB300_PAIR_BK>;
+// One work unit per pair (all tiles in one wave): sixteen epilogue warps, output staging in
+// the idle ring.
+using Pair1WCfg = gb300::PairConfig<256, GB300_PAIR_STAGES, 16, GB300_PAIR_BK, true>;
+#ifndef GB300_PAIR1W
+#define GB300_PAIR1W 1
+#endif
 // The same 128 x 256 tiles with sixteen epilogue warps (four per TMEM lane quarter, 64
 // columns each, 96 registers): the whole-tile kernel when all tiles fit one wave, where every
 // CTA's epilogue is an exposed tail that more warps shorten (2048^3 + bias + GELU, same box: 4
@@ -103,7 +109,10 @@ constexpr uint64_t kMinTimeoutNs = 1000000ull;
 // whole tiles, 23 us stream-K).
 constexpr int64_t kStreamKMinUnits = 16;
 constexpr int kSplitKMinBlocks = 8;   // split-K: k-blocks per CTA at least
-constexpr int kPairLongK = 8192;       // pairs for a one-wave problem from this K on
+#ifndef GB300_PAIR_LONG_K
+#define GB300_PAIR_LONG_K 8192
+#endif
+constexpr int kPairLongK = GB300_PAIR_LONG_K;   // pairs for a one-wave problem from this K on
 constexpr int kStreamKMinSpread = 2;
 
 }  // namespace
@@ -112,6 +121,7 @@ struct gemm_ctx {
     int device = -1;
     int num_sms = 0;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    bool pair1w_ok = false;   // the one-wave pair instance runs as many clusters at once
     uint32_t *d_err = nullptr;
     uint64_t timeout_ns = kDefaultTimeoutNs;
     int debug = 0;
@@ -289,7 +299,7 @@ void launch_pdl_cluster(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, gb
 // The kernel instance gemm_run launches for a problem, with its grid and the schedule fields
 // of its parameters. make_plan decides; launch runs the plan; gemm_describe reports it.
 enum PlanKind : int {
-    PLAN_PAIR, PLAN_TILES, PLAN_TILES16, PLAN_STREAMK, PLAN_SPLITK, PLAN_ROWCLUSTER, PLAN_ROWCLUSTER2
+    PLAN_PAIR, PLAN_PAIR1W, PLAN_TILES, PLAN_TILES16, PLAN_STREAMK, PLAN_SPLITK, PLAN_ROWCLUSTER, PLAN_ROWCLUSTER2
 };
 
 struct Plan {
@@ -306,6 +316,7 @@ const char *plan_kernel_name(PlanKind k)
 {
     switch (k) {
     case PLAN_PAIR: return "gemm_tcgen05_pair_kernel<PairConfig<256,3,4,128>>";
+    case PLAN_PAIR1W: return "gemm_tcgen05_pair_kernel<PairConfig<256,3,16,128,true>>";
     case PLAN_TILES: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_TILES>";
     case PLAN_TILES16: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,16,64,true,true>,SCHED_TILES>";
     case PLAN_STREAMK: return "gemm_tcgen05_kernel<KernelConfig<128,256,4,4>,SCHED_STREAM_K>";
@@ -393,6 +404,9 @@ Plan make_plan(const gemm_ctx *ctx, int M, int N, int K, int epilogue)
         const int last = pl.num_tiles % pairs;
         pl.pair_split_from = (last > 0 && 2 * last <= pairs) ? pl.num_tiles - last : pl.num_tiles;
         pl.pair_units = pl.pair_split_from + 2 * (pl.num_tiles - pl.pair_split_from);
+        // one unit per pair: the sixteen-warp instance, its output staged in the idle ring
+        if (GB300_PAIR1W && pl.pair_units <= pairs && ctx->pair1w_ok)
+            pl.kind = PLAN_PAIR1W;
         return pl;
     }
     pl.m_blocks = (M + Cfg::BM - 1) / Cfg::BM;
@@ -454,7 +468,13 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     const Plan pl = make_plan(ctx, M, N, K, epilogue);
     // K per ring stage of the chosen kernel: A goes in 64-wide boxes either way, B in boxes
     // of that many rows
-    const int bk = pl.kind == PLAN_PAIR ? PairCfg::BK : pl.kind == PLAN_TILES16 ? Cfg16::BK : Cfg::BK;
+    const int bk = (pl.kind == PLAN_PAIR || pl.kind == PLAN_PAIR1W) ? PairCfg::BK
+                   : pl.kind == PLAN_TILES16                      ? Cfg16::BK
+                                                                  : Cfg::BK;
+    static_assert(Pair1WCfg::BK == PairCfg::BK, "one B box height for both pair instances");
+    // Pair1WCfg stages its output in the operand ring: one unit per pair at most
+    if (pl.kind == PLAN_PAIR1W && pl.grid < 2 * pl.pair_units)
+        return GEMM_ERR_ARG;
     // Cfg16 stages its output in the operand ring: one tile per CTA at most
     if (pl.kind == PLAN_TILES16 && pl.grid < pl.num_tiles)
         return GEMM_ERR_ARG;
@@ -511,6 +531,10 @@ int launch(gemm_ctx *ctx, int M, int N, int K, const void *A, const void *B, con
     case PLAN_PAIR:
         launch_pdl(gb300::gemm_tcgen05_pair_kernel<PairCfg>, pl.grid, PairCfg::NUM_THREADS, PairCfg::SMEM_BYTES,
                    stream, ta, tb, tc, p);
+        break;
+    case PLAN_PAIR1W:
+        launch_pdl(gb300::gemm_tcgen05_pair_kernel<Pair1WCfg>, pl.grid, Pair1WCfg::NUM_THREADS,
+                   Pair1WCfg::SMEM_BYTES, stream, ta, tb, tc, p);
         break;
     case PLAN_SPLITK:
         launch_pdl_cluster(gb300::gemm_tcgen05_kernel<SplitCfg, gb300::SCHED_SPLIT_K>, pl.grid, pl.cluster,
@@ -616,6 +640,14 @@ int gemm_create(gemm_ctx **out, int device)
         int clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, gb300::gemm_tcgen05_pair_kernel<PairCfg>, &lc) == cudaSuccess)
             ctx->max_clusters = clusters;
+        // the one-wave instance: as many clusters at once, or it is not used
+        lc.blockDim = dim3(Pair1WCfg::NUM_THREADS, 1, 1);
+        lc.dynamicSmemBytes = Pair1WCfg::SMEM_BYTES;
+        clusters = 0;
+        if (cudaFuncSetAttribute(gb300::gemm_tcgen05_pair_kernel<Pair1WCfg>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Pair1WCfg::SMEM_BYTES) == cudaSuccess &&
+            cudaOccupancyMaxActiveClusters(&clusters, gb300::gemm_tcgen05_pair_kernel<Pair1WCfg>, &lc) == cudaSuccess)
+            ctx->pair1w_ok = clusters >= ctx->max_clusters;
     }
     cudaGetLastError();
     // Split-K clusters: how many clusters of 2, 4 and 8 CTAs fit at once (0: that size is not

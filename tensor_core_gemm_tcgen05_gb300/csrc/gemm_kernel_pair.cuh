@@ -28,7 +28,9 @@
 
 namespace gb300 {
 
-template <int BN_, int STAGES_, int EPI_WARPS_ = 4, int BK_ = 64>
+// STORE_IN_RING_: the output staging boxes overlay the operand ring (launches that give each
+// pair at most one work unit: the ring is idle once the accumulator is complete).
+template <int BN_, int STAGES_, int EPI_WARPS_ = 4, int BK_ = 64, bool STORE_IN_RING_ = false>
 struct PairConfig {
     static constexpr int CTA_BM = 128;     // rows per CTA (= TMEM lanes)
     static constexpr int BM = 256;         // rows per pair tile (= UMMA M)
@@ -42,6 +44,7 @@ struct PairConfig {
     static constexpr int A_ATOMS = BK / 64;
     static constexpr int UMMA_K = 16;
     static constexpr int STAGES = STAGES_;
+    static constexpr bool STORE_IN_RING = STORE_IN_RING_;
     static constexpr int A_BYTES = CTA_BM * BK * 2;
     static constexpr int B_BOX_N = 64;
     static constexpr int B_BOXES = CTA_BN / B_BOX_N;
@@ -55,13 +58,18 @@ struct PairConfig {
     static constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int BIAS_OFFSET = STAGES * STAGE_BYTES + ((NUM_BARS * 8 + 16 + 15) / 16) * 16;
-    static constexpr int STORE_OFFSET = ((BIAS_OFFSET + NUM_EPI_WARPS * BN * 2 + 1023) / 1024) * 1024;
-    static constexpr int SMEM_BYTES = 1024 + STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES;
+    static constexpr int BIAS_END = BIAS_OFFSET + NUM_EPI_WARPS * BN * 2;
+    static constexpr int STORE_OFFSET = STORE_IN_RING ? 0 : ((BIAS_END + 1023) / 1024) * 1024;
+    static constexpr int SMEM_BYTES =
+        1024 + (STORE_IN_RING ? BIAS_END : STORE_OFFSET + NUM_EPI_WARPS * EPI_STORE_WARP_BYTES);
 
     static_assert(BN % 128 == 0 && BN >= 128 && BN <= 256, "UMMA N for M = 256, two 64-column boxes per CTA");
     static_assert(BK == 64 || BK == 128, "one or two A atoms per stage; B boxes BK rows tall");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM alloc size");
-    static_assert(NUM_EPI_WARPS == 4 || NUM_EPI_WARPS == 8, "one or two warps per TMEM lane quarter");
+    static_assert(NUM_EPI_WARPS == 4 || NUM_EPI_WARPS == 8 || NUM_EPI_WARPS == 16,
+                  "one, two or four warps per TMEM lane quarter");
+    static_assert(!STORE_IN_RING || NUM_EPI_WARPS * EPI_STORE_WARP_BYTES <= STAGES * STAGE_BYTES,
+                  "output staging fits the operand ring");
     static_assert((BN / 32) % EPI_COL_GROUPS == 0, "column chunks split evenly between warps");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 };

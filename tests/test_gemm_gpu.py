@@ -423,21 +423,29 @@ def test_clock_trace_beside_a_gemm(ctx):
         g.gemm_clock_trace(ctx, trace, n, 10, 5_000_000, side)   # interval below 1 us
 
 
-@pytest.mark.parametrize("force", ["single", "pair"])
+@pytest.mark.parametrize("force", ["single", "pair", "pair_one_unit"])
 def test_bounded_wait_reports_timeout_and_context_survives(ctx, force):
     """The producer withholds its first operand load, so the MMA warp's wait runs out:
     the kernel must return (no hang, no fault) and report GEMM_ERR_TIMEOUT; afterwards the
-    same context computes correct results again."""
-    if force == "pair" and g.gemm_num_pairs(ctx) == 0:
+    same context computes correct results again. "pair" has more work units than pairs (the
+    four-warp instance), "pair_one_unit" one tile (the sixteen-warp instance)."""
+    pairs = g.gemm_num_pairs(ctx)
+    if force != "single" and pairs == 0:
         pytest.skip("the pair kernel cannot run on this device")
     flag = g.GEMM_DEBUG_FORCE_SINGLE if force == "single" else g.GEMM_DEBUG_FORCE_PAIR
+    M, N = (256 * (pairs + 1), 256) if force == "pair" else (256, 256)
     g.gemm_set_timeout_ns(ctx, 20_000_000)
     g.gemm_set_debug(ctx, g.GEMM_DEBUG_WITHHOLD_FIRST_LOAD | flag)
     try:
+        desc = g.gemm_describe(ctx, M, N, 64, g.EPI_NONE)
+        if force == "pair":
+            assert "PairConfig<256,3,4,128>" in desc, desc
+        elif force == "pair_one_unit":
+            assert "PairConfig<256,3,16,128,true>" in desc, desc
         dev = torch.device("cuda:0")
-        A = torch.ones(256, 64, dtype=torch.float16, device=dev)
-        B = torch.ones(64, 256, dtype=torch.float16, device=dev)
-        C = torch.zeros(256, 256, dtype=torch.float16, device=dev)
+        A = torch.ones(M, 64, dtype=torch.float16, device=dev)
+        B = torch.ones(64, N, dtype=torch.float16, device=dev)
+        C = torch.zeros(M, N, dtype=torch.float16, device=dev)
         g.gemm(ctx, A, B, None, g.EPI_NONE, out=C)
         torch.cuda.synchronize()
         status, detail = g.gemm_last_device_error(ctx)
@@ -549,6 +557,28 @@ def test_pair_last_round_in_n_halves(ctx, epi, with_bias):
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
     assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 128), (300, 520, 1000), (700, 264, 4104)],
+                         ids=lambda v: "x".join(map(str, v)))
+def test_pair_instance_with_one_unit_per_pair(ctx, shape):
+    """With no more work units than pairs the pair kernel runs its sixteen-warp instance,
+    whose output staging lies in the operand ring: B = I gives A exactly, and GELU + bias
+    matches the oracle with rows and columns past C in the last tiles."""
+    if g.gemm_num_pairs(ctx) == 0:
+        pytest.skip("the pair kernel cannot run on this device")
+    M, N, K = shape
+    g.gemm_set_debug(ctx, g.GEMM_DEBUG_FORCE_PAIR)
+    try:
+        assert "PairConfig<256,3,16,128,true>" in g.gemm_describe(ctx, M, N, K, g.EPI_GELU)
+        if N <= K:
+            A = inputs.random_fp16((M, K), 31 + K)
+            C = run_guarded(ctx, A, torch.eye(K, N, dtype=torch.float16), None, g.EPI_NONE)
+            assert torch.equal(C, A[:, :N])
+        check(ctx, M, N, K, epi=g.EPI_GELU, with_bias=True, seed=M + N)
+        assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+    finally:
+        g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
 
 
 def test_long_k_one_wave_runs_on_pairs(ctx):
