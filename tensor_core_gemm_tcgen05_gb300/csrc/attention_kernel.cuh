@@ -398,10 +398,24 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmap_q);
-        tma_prefetch_desc(&tmap_k);
-        tma_prefetch_desc(&tmap_v);
         tma_prefetch_desc(&tmap_o);
+        // Q and the first key/value block go out before the Tensor Memory allocation and the
+        // block barrier, so that their latency overlaps the rest of the set-up (the barriers
+        // are initialised and fenced above; the wait orders the reads after the previous grid)
+        grid_dependency_wait();
+        mbar_arrive_expect_tx(q_full, Cfg::TILES * TILE);
+        for (int t = 0; t < Cfg::TILES; ++t) {
+            tma_load_3d(sQ + t * TILE, &tmap_q, q_full, 0, q0 + t * Cfg::BQ, h);
+            tma_load_3d(sQ + t * TILE + ATOM, &tmap_q, q_full, 64, q0 + t * Cfg::BQ, h);
+        }
+        if (n_kv > 0) {
+            const uint32_t fb = kv_full0, sK = sKV, sV = sKV + TILE;
+            mbar_arrive_expect_tx(fb, 2 * TILE);
+            tma_load_3d(sK, &tmap_k, fb, 0, 0, h);
+            tma_load_3d(sK + ATOM, &tmap_k, fb, 64, 0, h);
+            tma_load_3d(sV, &tmap_v, fb, 0, 0, h);
+            tma_load_3d(sV + ATOM, &tmap_v, fb, 64, 0, h);
+        }
     }
     if (warp == 1) {
         tmem_alloc<1>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -418,14 +432,10 @@ __global__ void __launch_bounds__(AttnConfig::NUM_THREADS, 1)
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, Cfg::TILES * TILE);
-            for (int t = 0; t < Cfg::TILES; ++t) {
-                tma_load_3d(sQ + t * TILE, &tmap_q, q_full, 0, q0 + t * Cfg::BQ, h);
-                tma_load_3d(sQ + t * TILE + ATOM, &tmap_q, q_full, 64, q0 + t * Cfg::BQ, h);
-            }
+            // Q and key/value block 0 were issued during the set-up (stage 0, phase 0)
             bool ok = true;
-            uint32_t issued = 0, issued_parity = 0;
-            for (int j = 0; j < n_kv; ++j) {
+            uint32_t issued = n_kv > 0 ? 1u : 0u, issued_parity = 0;
+            for (int j = 1; j < n_kv; ++j) {
                 const int s = j & 1;
                 const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
                 if (!wait_bounded(kv_empty0 + 8u * s, ph ^ 1u, wc, ERR_PRODUCER_SLOT)) {
