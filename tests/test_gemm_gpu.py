@@ -605,6 +605,44 @@ def test_long_k_one_wave_runs_on_pairs(ctx):
     assert_parity(C.numpy()[rows], oracle_ref(A, B, bias, g.EPI_GELU, rows=rows), "long-K pair")
 
 
+def _random_shapes(seed, n, m_max, n_max, k_max):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        M = int(rng.integers(1, m_max + 1))
+        N = 8 * int(rng.integers(1, n_max // 8 + 1))
+        K = 8 * int(rng.integers(0, k_max // 8 + 1))
+        epi = int(rng.choice([g.EPI_NONE, g.EPI_GELU, g.EPI_RELU]))
+        out.append((M, N, K, epi, bool(rng.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("schedule", ["default", "single", "pair", "splitk", "streamk"])
+def test_random_shapes_against_the_oracle(ctx, schedule):
+    """Seeded random problems (ragged M, N and K, K = 0 included, every epilogue, with and
+    without bias) under the planner's own choice and under each forced schedule: sampled rows,
+    the last ones included, against the oracle, guard rows and tail untouched."""
+    if schedule == "pair" and g.gemm_num_pairs(ctx) == 0:
+        pytest.skip("the pair kernel cannot run on this device")
+    big = schedule == "default"
+    shapes = _random_shapes({"default": 71, "single": 72, "pair": 73, "splitk": 74, "streamk": 75}[schedule],
+                            40 if big else 24, 6000 if big else 1500, 6000 if big else 1500, 9000 if big else 4000)
+    if schedule != "default":
+        g.gemm_set_debug(ctx, FORCE[schedule])
+    try:
+        for i, (M, N, K, epi, with_bias) in enumerate(shapes):
+            A = inputs.random_fp16((M, K), 8000 + i, k=max(K, 1))
+            B = inputs.random_fp16((K, N), 8100 + i, k=max(K, 1))
+            bias = inputs.random_fp16((N,), 8200 + i) if with_bias else None
+            C = run_guarded(ctx, A, B, bias, epi)
+            rows = inputs.sample_rows(M, 24, seed=60 + i, include_last=3).numpy()
+            what = f"{schedule} {M}x{N}x{K} epi={epi} bias={with_bias}: {g.gemm_describe(ctx, M, N, K, epi)}"
+            assert_parity(C.numpy()[rows], oracle_ref(A, B, bias, epi, rows=rows), what)
+        assert g.gemm_last_device_error(ctx) == (g.GEMM_OK, 0)
+    finally:
+        g.gemm_set_debug(ctx, g.GEMM_DEBUG_NONE)
+
+
 def test_splitk_in_host_column_bands(ctx):
     """Split-K inside gemm_run_host's column bands: each band's C is a slice of a wider
     matrix (row stride N, not the band's width), which split-K writes directly."""
