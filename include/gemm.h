@@ -99,7 +99,10 @@ int gemm_create(gemm_ctx **out, int device);
  * Ownership: the caller owns every buffer and must keep them alive until the stream has
  * passed this call. gemm_run allocates nothing and launches exactly one kernel.
  * Schedule: 256 x 256 tiles on CTA pairs when there are at least as many as co-resident
- * pairs; otherwise 128 x 256 tiles on single SMs. When those tiles leave most SMs idle:
+ * pairs, or when K >= 8192, at least three quarters of the pairs get a tile and the
+ * single-SM tiles would fit one wave; otherwise 128 x 256 tiles on single SMs. On pairs, a
+ * last round of tiles that at most half of the pairs would work on runs as 256 x 128
+ * halves, one per pair. When the single-SM tiles leave most SMs idle:
  * split-K, a cluster of S = 8, 4 or 2 CTAs per tile (the largest S with tiles x S <= SMs,
  * all clusters co-resident, and at least 8 k-blocks of 64 per CTA), each CTA summing 1/S of
  * the k-blocks; the S FP32 partials are added over distributed shared memory in a fixed
